@@ -1,0 +1,235 @@
+/*
+ * pa.h -- C ABI of libpa.so, a PagedAttention forward pass for one GB300 GPU.
+ *
+ * What the library computes
+ * -------------------------
+ * PagedAttentionOperation, "Constraints": softmax attention of a batch of
+ * query tokens over a KV cache kept as fixed-size blocks. For sequence b,
+ * query token i in [0, q_b) and head h in [0, H):
+ *
+ *   G      = H / Hk                         (GQA: H % Hk == 0)
+ *   kvh    = h / G                          (contiguous head groups)
+ *   p      = L_b - q_b + i                  (prefix = max(0, L_b - q_b), the
+ *                                            mask-alignment rule of the
+ *                                            MASK_TYPE_NORM_COMPRESS bullets)
+ *   K_b[j] = key_cache  [block_tables[b][j / bs], j % bs, kvh, :]
+ *   V_b[j] = value_cache[block_tables[b][j / bs], j % bs, kvh, :]
+ *   s_j    = scale * <q[b,i,h,:], K_b[j]> + bias(h, i, j),   j in [0, L_b)
+ *   out[b,i,h,:] = sum_j softmax(s)_j * V_b[j]
+ *
+ * where L_b = context_lens[b] counts the whole KV length including the
+ * current query tokens, and bias is
+ *   PA_MASK_NONE           0
+ *   PA_MASK_ALIBI          alibi_slopes[h] * (j - p)
+ *   PA_MASK_NORM_COMPRESS  sigma = max(0, L_b - 2048);
+ *                          0 if j < sigma, else mask[p - sigma][j - sigma]
+ *                          (the shared 2048 x 2048 causal mask: strict upper
+ *                          triangle a large negative fill, diagonal and lower
+ *                          triangle 0; the shift keeps both indices inside the
+ *                          mask for any L_b, so sequences longer than 2048 need
+ *                          nothing extra from the caller).
+ * The mask value is added to the scaled score, not substituted by -inf, and is
+ * not scaled. The kernels read the mask only where j > L_b - q_b: every other
+ * element they would read lies on or below the diagonal, which the pages fix
+ * at 0.
+ *
+ * The split-KV path follows SparseAttnSharedkvMetadata ("功能说明" and the
+ * `metadata` output): a task list gives each CTA its (batch, head group, query
+ * tile, KV-block range); CTAs that cover part of a sequence's KV write a
+ * partial result, and a reduction pass merges the partials by log-sum-exp.
+ *
+ * Conventions
+ * -----------
+ * - Every function returns a pa_status; nothing is thrown across the ABI.
+ * - pa_plan is pure host code. pa_forward is asynchronous on the caller's
+ *   stream, allocates nothing and never synchronises.
+ * - Tensors are dense row-major; fp16 is IEEE binary16. "device" pointers are
+ *   CUDA global memory of the current device; the caller owns all memory.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,      /* a constraint of the pages or of this ABI is violated */
+  PA_ERR_UNSUPPORTED = 2,      /* a valid mode this build does not implement */
+  PA_ERR_BUFFER_TOO_SMALL = 3, /* work/combine capacity or workspace too small */
+  PA_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+  PA_ERR_BLOCK_INDEX = 5,      /* a device-side block-table entry outside [0, num_blocks) */
+  PA_ERR_TIMEOUT = 6           /* a bounded device-side wait ran out */
+} pa_status;
+
+/* Mask types. 5 is MASK_TYPE_NORM_COMPRESS as numbered by the pages; the
+ * pages name UNDEFINED, NORM and ALIBI without numbers, so 0/1/2 are ours.
+ * 1 (full mask of the real max_seq_len) and 4 (a spec-decoding mask whose
+ * contents the pages do not describe) return PA_ERR_UNSUPPORTED. */
+typedef enum pa_mask_type {
+  PA_MASK_NONE = 0,
+  PA_MASK_NORM = 1,
+  PA_MASK_ALIBI = 2,
+  PA_MASK_SPEC = 4,
+  PA_MASK_NORM_COMPRESS = 5
+} pa_mask_type;
+
+#define PA_COMPRESS_MASK_SIZE 2048
+#define PA_MAX_BATCH 2048
+#define PA_MAX_HEAD_SIZE 576
+#define PA_FMA_MAX_ROWS 8
+#define PA_TC_TILE_ROWS 64
+#define PA_STATUS_BYTES 256
+
+/* Status bits written by the kernels into the first word of the workspace. */
+#define PA_STATUS_BIT_BLOCK_INDEX 1u
+#define PA_STATUS_BIT_TIMEOUT 2u
+#define PA_STATUS_BIT_WORKSPACE 4u
+
+/*
+ * Problem description shared by pa_plan and pa_forward.
+ *
+ *   batch               B, 0 < B <= 2048 (PagedAttentionOperation "Constraints")
+ *   num_heads           H > 0
+ *   kv_heads            Hk > 0, H % Hk == 0 (GQA condition of both pages)
+ *   head_size_k/_v      hk, hv in (0, 576] and multiples of 16; a size above
+ *                       256 needs block_size <= 128 ("Constraints")
+ *   block_size          bs, a multiple of 16; <= 128 when max_seqlen_q > 1
+ *                       (parallel decoding)
+ *   num_blocks          physical blocks in each cache
+ *   max_blocks_per_seq  row length of block_tables, >= ceil(max L_b / bs)
+ *   max_seqlen_q        largest q_b (0 is read as 1); the max_seqlen_q
+ *                       attribute of SparseAttnSharedkvMetadata
+ *   mask_type           a pa_mask_type
+ *   chunk_blocks        KV blocks per split, > 0; or 0 for the automatic rule
+ *   num_sms             streaming multiprocessors of the target GPU (> 0 when
+ *                       chunk_blocks == 0)
+ *   scale               QK scale; <= 0 selects 1/sqrt(hk) (SCALE_TYPE_TOR)
+ */
+typedef struct pa_config {
+  int32_t batch;
+  int32_t num_heads;
+  int32_t kv_heads;
+  int32_t head_size_k;
+  int32_t head_size_v;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t max_seqlen_q;
+  int32_t mask_type;
+  int32_t chunk_blocks;
+  int32_t num_sms;
+  float scale;
+} pa_config;
+
+/*
+ * The work list (the `metadata` of SparseAttnSharedkvMetadata, restated).
+ *
+ * Rows. The query rows of one (b, kvh) pair are R_b = G * q_b rows ordered
+ * token-major: row r is query token i = r / G of head h = kvh * G + r % G.
+ * A launch uses one tile height TR for every sequence:
+ *   TR = G * max_seqlen_q   if that is <= PA_FMA_MAX_ROWS (CUDA-core path)
+ *   TR = PA_TC_TILE_ROWS    otherwise                      (tensor-core path)
+ * and sequence b has QT_b = ceil(R_b / TR) tiles; tile qt covers rows
+ * [qt * TR, min(R_b, (qt + 1) * TR)).
+ *
+ * Chunk. NB_b = ceil(L_b / bs). With chunk_blocks > 0, c = chunk_blocks.
+ * Otherwise
+ *   W     = sum_b NB_b * Hk * QT_b
+ *   c_bal = ceil(W / (8 * num_sms))
+ *   c_min = ceil(64 * TR * hv / (bs * (hk + hv)))
+ *   c     = max(1, c_bal, c_min)
+ * (c_bal aims at about eight work items per SM so that variable lengths
+ * balance; c_min keeps the partial results that a split writes and re-reads
+ * below about a sixteenth of the KV bytes of the split.)
+ * Sequence b has S_b = ceil(NB_b / c) splits; split s covers KV blocks
+ * [s * c, min(NB_b, (s + 1) * c)).
+ *
+ * Items. One item per (b, kvh, qt, s), in lexicographic order of that tuple
+ * (b slowest, s fastest); CTA x of the attention kernel runs item x. Each item
+ * is PA_WORK_INTS int32:
+ *   [0] b          [1] kvh        [2] row_begin   [3] row_end
+ *   [4] kb_begin   [5] kb_end     [6] q_start     [7] slot
+ * row_begin/row_end are the tile's row range, q_start = sum_{b' < b} q_b' is
+ * the index of the sequence's first query token, and slot is -1 when S_b == 1
+ * (the item writes `out` directly) or else the index of the first partial row
+ * the item writes. Partial rows are numbered consecutively in item order over
+ * the items with S_b > 1, each such item taking row_end - row_begin rows, so
+ * the S_b splits of one tile sit at slot_0 + s * (row_end - row_begin).
+ *
+ * Combine entries. One per (b, kvh, qt) with S_b > 1, in the same order; each
+ * is PA_COMBINE_INTS int32:
+ *   [0] b   [1] kvh   [2] first_item (index of split 0's item)   [3] S_b
+ *
+ * Workspace. PA_STATUS_BYTES of status first (word 0 collects PA_STATUS_BIT_*
+ * flags), then P * hv fp32 partial outputs (already divided by their softmax
+ * sum), then P fp32 log-sum-exps in natural-log units, where P is the number
+ * of partial rows; each part starts on a 256-byte boundary.
+ */
+#define PA_WORK_INTS 8
+#define PA_COMBINE_INTS 4
+
+/*
+ * pa_plan -- validate a batch and build its work list (host only).
+ *
+ * context_lens  host int32 [batch], 1 <= q_b <= L_b.
+ * q_seqlens     host int32 [batch], 1 <= q_b <= max(1, max_seqlen_q); NULL
+ *               means every q_b = 1. With NORM_COMPRESS q_b <= 2048.
+ * work          host int32 [work_cap * PA_WORK_INTS], or NULL to query sizes.
+ * combine       host int32 [comb_cap * PA_COMBINE_INTS], or NULL.
+ * n_items, n_combine, workspace_bytes   outputs (may be NULL).
+ * Returns PA_ERR_BUFFER_TOO_SMALL (after writing the counts) when a non-NULL
+ * buffer is too small. Writes nothing else on error.
+ */
+pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens, const int32_t* q_seqlens,
+                  int32_t* work, int64_t work_cap, int64_t* n_items,
+                  int32_t* combine, int64_t comb_cap, int64_t* n_combine,
+                  size_t* workspace_bytes);
+
+/*
+ * pa_forward -- run attention for one planned batch (device, asynchronous).
+ *
+ * query         device fp16 [sum q_b, H, hk]
+ * key_cache     device fp16 [num_blocks, bs, Hk, hk]; 16-byte aligned
+ * value_cache   device fp16 [num_blocks, bs, Hk, hv]; 16-byte aligned
+ * block_tables  device int32 [batch, max_blocks_per_seq]
+ * context_lens  device int32 [batch]
+ * q_seqlens     device int32 [batch], or NULL when every q_b = 1
+ * mask          device fp16 [2048, 2048]; non-NULL exactly for NORM_COMPRESS
+ * alibi_slopes  device fp32 [H]; non-NULL exactly for ALIBI
+ * work/combine  device copies of pa_plan's lists (same cfg, same lengths)
+ * workspace     device, >= pa_plan's workspace_bytes, 256-byte aligned; its
+ *               status word must be zero before the first call (see
+ *               pa_status_clear) and is only ever OR-ed by the kernels
+ * out           device fp16 [sum q_b, H, hv]
+ * stream        a cudaStream_t (NULL = legacy default stream)
+ *
+ * Host-side errors return before anything is enqueued. Block-table entries
+ * outside [0, num_blocks) are never dereferenced: the kernel reads zeros in
+ * their place and sets PA_STATUS_BIT_BLOCK_INDEX, which pa_status_read reports.
+ */
+pa_status pa_forward(const pa_config* cfg, const void* query, const void* key_cache,
+                     const void* value_cache, const int32_t* block_tables,
+                     const int32_t* context_lens, const int32_t* q_seqlens, const void* mask,
+                     const float* alibi_slopes, const int32_t* work, int64_t n_items,
+                     const int32_t* combine, int64_t n_combine, void* workspace,
+                     size_t workspace_bytes, void* out, void* stream);
+
+/* Zero the status word of a workspace (enqueued on stream). */
+pa_status pa_status_clear(void* workspace, void* stream);
+
+/* Wait for stream, read the status word into *bits (may be NULL) and map it to
+ * PA_OK, PA_ERR_TIMEOUT, PA_ERR_BLOCK_INDEX or PA_ERR_BUFFER_TOO_SMALL. */
+pa_status pa_status_read(const void* workspace, void* stream, uint32_t* bits);
+
+/* Static description of a status code. */
+const char* pa_status_string(pa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

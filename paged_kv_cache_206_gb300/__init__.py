@@ -1,0 +1,237 @@
+"""Python binding of libpa.so: GB300 PagedAttention forward.
+
+The functions here marshal arguments to the C ABI declared in
+``include/pa.h`` and raise :class:`PaError` on a non-OK status; every step of
+the computation runs in the library's CUDA kernels. Device buffers are torch
+tensors (torch supplies device memory and streams only). There is no CPU
+fallback: if ``libpa.so`` has not been built, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+from .build_lib import LIB
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_BUFFER_TOO_SMALL = 3
+PA_ERR_CUDA = 4
+PA_ERR_BLOCK_INDEX = 5
+PA_ERR_TIMEOUT = 6
+
+PA_MASK_NONE = 0
+PA_MASK_NORM = 1
+PA_MASK_ALIBI = 2
+PA_MASK_SPEC = 4
+PA_MASK_NORM_COMPRESS = 5
+
+PA_WORK_INTS = 8
+PA_COMBINE_INTS = 4
+PA_STATUS_BYTES = 256
+
+# Every symbol include/pa.h declares.
+EXPORTS = ("pa_plan", "pa_forward", "pa_status_clear", "pa_status_read", "pa_status_string")
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class pa_config(ctypes.Structure):
+    """Mirror of ``pa_config`` in include/pa.h."""
+
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("kv_heads", ctypes.c_int32),
+        ("head_size_k", ctypes.c_int32),
+        ("head_size_v", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32),
+        ("max_seqlen_q", ctypes.c_int32),
+        ("mask_type", ctypes.c_int32),
+        ("chunk_blocks", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libpa.so (built by ``build_lib.build``); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: run paged_kv_cache_206_gb300.build_lib.build() "
+                           "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    cfgp = ctypes.POINTER(pa_config)
+    lib.pa_plan.restype = ctypes.c_int
+    lib.pa_plan.argtypes = [cfgp, P, P, P, i64, P, P, i64, P, P]
+    lib.pa_forward.restype = ctypes.c_int
+    lib.pa_forward.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, i64, P, i64, P, sz, P, P]
+    lib.pa_status_clear.restype = ctypes.c_int
+    lib.pa_status_clear.argtypes = [P, P]
+    lib.pa_status_read.restype = ctypes.c_int
+    lib.pa_status_read.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_status_string.argtypes = [ctypes.c_int]
+    if path == LIB:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().pa_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != PA_OK:
+        raise PaError(status, where)
+
+
+def make_config(*, batch, num_heads, kv_heads, head_size_k, head_size_v=None, block_size,
+                num_blocks, max_blocks_per_seq, max_seqlen_q=1, mask_type=PA_MASK_NONE,
+                chunk_blocks=0, num_sms=0, scale=0.0) -> pa_config:
+    return pa_config(int(batch), int(num_heads), int(kv_heads), int(head_size_k),
+                     int(head_size_k if head_size_v is None else head_size_v), int(block_size),
+                     int(num_blocks), int(max_blocks_per_seq), int(max_seqlen_q),
+                     int(mask_type), int(chunk_blocks), int(num_sms), float(scale))
+
+
+def config_for(w, num_sms: int = 0, chunk_blocks: int | None = None) -> pa_config:
+    """pa_config of a ``workloads.Workload``."""
+    return make_config(batch=w.batch, num_heads=w.num_heads, kv_heads=w.kv_heads,
+                       head_size_k=w.head_size_k, head_size_v=w.head_size_v,
+                       block_size=w.block_size, num_blocks=w.num_blocks,
+                       max_blocks_per_seq=w.max_blocks_per_seq, max_seqlen_q=w.max_seqlen_q,
+                       mask_type=w.mask_type,
+                       chunk_blocks=w.chunk_blocks if chunk_blocks is None else chunk_blocks,
+                       num_sms=num_sms, scale=w.scale)
+
+
+@dataclass
+class Plan:
+    work: np.ndarray  # int32 [n_items, 8]
+    combine: np.ndarray  # int32 [n_combine, 4]
+    workspace_bytes: int
+
+
+def _np_ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def pa_plan(cfg: pa_config, context_lens, q_seqlens=None) -> Plan:
+    """Host planner (pa_plan): validate and build the work and combine lists."""
+    lib = load_library()
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    ql = None if q_seqlens is None else np.ascontiguousarray(q_seqlens, dtype=np.int32)
+    n_items, n_comb, ws = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_size_t()
+    _check(lib.pa_plan(ctypes.byref(cfg), _np_ptr(cl), _np_ptr(ql), None, 0, ctypes.byref(n_items),
+                       None, 0, ctypes.byref(n_comb), ctypes.byref(ws)), "pa_plan")
+    work = np.zeros((n_items.value, PA_WORK_INTS), dtype=np.int32)
+    comb = np.zeros((max(n_comb.value, 0), PA_COMBINE_INTS), dtype=np.int32)
+    _check(lib.pa_plan(ctypes.byref(cfg), _np_ptr(cl), _np_ptr(ql), _np_ptr(work), n_items.value,
+                       ctypes.byref(n_items), _np_ptr(comb), n_comb.value, ctypes.byref(n_comb),
+                       ctypes.byref(ws)), "pa_plan")
+    return Plan(work, comb, int(ws.value))
+
+
+def _tptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def pa_forward(cfg: pa_config, query, key_cache, value_cache, block_tables, context_lens,
+               q_seqlens, mask, alibi_slopes, work, combine, workspace, out, stream=None) -> None:
+    """Enqueue attention (pa_forward). All tensor arguments are CUDA tensors
+    (``q_seqlens``, ``mask``, ``alibi_slopes`` and ``combine`` may be None)."""
+    lib = load_library()
+    n_items = 0 if work is None else work.shape[0]
+    n_comb = 0 if combine is None else combine.shape[0]
+    st = lib.pa_forward(ctypes.byref(cfg), _tptr(query), _tptr(key_cache), _tptr(value_cache),
+                        _tptr(block_tables), _tptr(context_lens), _tptr(q_seqlens), _tptr(mask),
+                        _tptr(alibi_slopes), _tptr(work), n_items,
+                        _tptr(combine) if n_comb else None, n_comb, _tptr(workspace),
+                        workspace.numel() * workspace.element_size(), _tptr(out),
+                        _stream_handle(stream))
+    _check(st, "pa_forward")
+
+
+def pa_status_clear(workspace, stream=None) -> None:
+    _check(load_library().pa_status_clear(_tptr(workspace), _stream_handle(stream)),
+           "pa_status_clear")
+
+
+def pa_status_read(workspace, stream=None) -> tuple[int, int]:
+    """(status, bits): waits for the stream and reads the kernels' status word."""
+    bits = ctypes.c_uint32()
+    st = load_library().pa_status_read(_tptr(workspace), _stream_handle(stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+class DeviceBatch:
+    """A workload's tensors on one CUDA device, planned and ready to run.
+
+    Holds the device copies of the inputs, the work and combine lists, the
+    workspace (status word cleared) and the output buffer.
+    """
+
+    def __init__(self, w, device="cuda", num_sms: int | None = None,
+                 chunk_blocks: int | None = None):
+        import torch
+        dev = torch.device(device)
+        if num_sms is None:
+            num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.w = w
+        self.cfg = config_for(w, num_sms=num_sms, chunk_blocks=chunk_blocks)
+        ql_host = None if np.all(w.q_seqlens == 1) else w.q_seqlens
+        self.plan = pa_plan(self.cfg, w.context_lens, ql_host)
+
+        def up(a, dtype=None):
+            if a is None:
+                return None
+            t = torch.from_numpy(np.ascontiguousarray(a))
+            return t.to(dev, non_blocking=False)
+
+        self.query = up(w.query)
+        self.key_cache = up(w.key_cache)
+        self.value_cache = up(w.value_cache)
+        self.block_tables = up(w.block_tables)
+        self.context_lens = up(w.context_lens)
+        self.q_seqlens = up(ql_host)
+        self.mask = up(w.mask)
+        self.alibi_slopes = up(w.alibi_slopes)
+        self.work = up(self.plan.work)
+        self.combine = up(self.plan.combine) if self.plan.combine.shape[0] else None
+        ws = max(self.plan.workspace_bytes, PA_STATUS_BYTES)
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
+        self.out = torch.empty((w.total_q, w.num_heads, w.head_size_v), dtype=torch.float16,
+                               device=dev)
+
+    def forward(self, stream=None):
+        pa_forward(self.cfg, self.query, self.key_cache, self.value_cache, self.block_tables,
+                   self.context_lens, self.q_seqlens, self.mask, self.alibi_slopes, self.work,
+                   self.combine, self.workspace, self.out, stream)
+        return self.out
+
+    def status(self, stream=None):
+        return pa_status_read(self.workspace, stream)

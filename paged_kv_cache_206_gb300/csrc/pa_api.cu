@@ -1,0 +1,201 @@
+// C ABI of libpa.so: argument checks, TMA descriptors and kernel launches.
+// The operation and its constraints are those of PagedAttentionOperation
+// ("Constraints"); the work list is built by pa_plan (pa_plan.cpp).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_combine.cuh"
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+template <int RT>
+cudaError_t launch_fma(const CUtensorMap&, const CUtensorMap&, const FwdParams&, int64_t,
+                       cudaStream_t);
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+struct BoxGeom {
+  int width;  // elements per row of one TMA box
+  uint32_t swz_mask;
+  CUtensorMapSwizzle swizzle;
+};
+
+// Widest box (<= 128 bytes) that divides the head size, with the matching
+// swizzle so that reads of one 16-byte chunk column across rows hit distinct
+// shared-memory banks.
+BoxGeom box_geom(int head_size) {
+  if (head_size % 64 == 0) return {64, 7u, CU_TENSOR_MAP_SWIZZLE_128B};
+  if (head_size % 32 == 0) return {32, 3u, CU_TENSOR_MAP_SWIZZLE_64B};
+  return {16, 1u, CU_TENSOR_MAP_SWIZZLE_32B};
+}
+
+// The cache [num_blocks, bs, Hk, hs] viewed as a 2-D tensor of
+// num_blocks * bs token rows by Hk * hs elements; a box is box_rows tokens of
+// one box-width slice of one kv head.
+bool cache_map(CUtensorMap* m, const void* base, const pa_config& c, int hs, int box_rows,
+               const BoxGeom& g) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cuuint64_t(c.kv_heads) * hs, cuuint64_t(c.num_blocks) * c.block_size};
+  cuuint64_t strides[1] = {cuuint64_t(c.kv_heads) * hs * 2};
+  cuuint32_t box[2] = {cuuint32_t(g.width), cuuint32_t(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, g.swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const void* key_cache,
+                                const void* value_cache, const int32_t* block_tables,
+                                const int32_t* context_lens, const int32_t* q_seqlens,
+                                const void* mask, const float* alibi_slopes, const int32_t* work,
+                                int64_t n_items, const int32_t* combine, int64_t n_combine,
+                                void* workspace, size_t workspace_bytes, void* out,
+                                void* stream_) {
+  using namespace pa;
+  pa_status st = validate_config(cfg);
+  if (st != PA_OK) return st;
+  const pa_config& c = *cfg;
+  if (!query || !key_cache || !value_cache || !block_tables || !context_lens || !out ||
+      !workspace)
+    return PA_ERR_INVALID_ARG;
+  if ((c.mask_type == PA_MASK_NORM_COMPRESS) != (mask != nullptr)) return PA_ERR_INVALID_ARG;
+  if ((c.mask_type == PA_MASK_ALIBI) != (alibi_slopes != nullptr)) return PA_ERR_INVALID_ARG;
+  if (n_items < 0 || n_combine < 0 || n_items > INT32_MAX || n_combine > INT32_MAX)
+    return PA_ERR_INVALID_ARG;
+  if ((n_items > 0 && !work) || (n_combine > 0 && !combine)) return PA_ERR_INVALID_ARG;
+  if (!aligned(query, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+      !aligned(out, 16) || !aligned(workspace, 256))
+    return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < PA_STATUS_BYTES) return PA_ERR_BUFFER_TOO_SMALL;
+  if (n_items == 0) return PA_OK;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const int64_t TR = tile_rows(c);
+  const int hk = c.head_size_k, hv = c.head_size_v;
+  const int64_t cap = workspace_rows(workspace_bytes, hv);
+  const WorkspaceLayout wl = workspace_layout(cap, hv);
+
+  FwdParams P{};
+  P.query = static_cast<const __half*>(query);
+  P.block_tables = block_tables;
+  P.context_lens = context_lens;
+  P.q_seqlens = q_seqlens;
+  P.mask = static_cast<const __half*>(mask);
+  P.alibi_slopes = alibi_slopes;
+  P.work = work;
+  P.out = static_cast<__half*>(out);
+  P.status = static_cast<uint32_t*>(workspace);
+  P.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.partial_o);
+  P.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.partial_lse);
+  P.part_rows_cap = cap;
+  P.num_heads = c.num_heads;
+  P.kv_heads = c.kv_heads;
+  P.group = c.num_heads / c.kv_heads;
+  P.hk = hk;
+  P.hv = hv;
+  P.block_size = c.block_size;
+  P.max_blocks_per_seq = c.max_blocks_per_seq;
+  P.num_blocks = c.num_blocks;
+  P.mask_type = c.mask_type;
+  const float scale = c.scale > 0.f ? c.scale : 1.0f / std::sqrt(float(hk));
+  P.scale_log2 = scale * kLog2e;
+
+  cudaError_t err;
+  if (TR <= PA_FMA_MAX_ROWS) {
+    const BoxGeom kg = box_geom(hk), vg = box_geom(hv);
+    P.kbw = kg.width;
+    P.vbw = vg.width;
+    P.kswz = kg.swz_mask;
+    P.vswz = vg.swz_mask;
+    CUtensorMap tmk, tmv;
+    if (!cache_map(&tmk, key_cache, c, hk, 16, kg) || !cache_map(&tmv, value_cache, c, hv, 16, vg))
+      return PA_ERR_CUDA;
+    switch (TR) {
+      case 1: err = launch_fma<1>(tmk, tmv, P, n_items, stream); break;
+      case 2: err = launch_fma<2>(tmk, tmv, P, n_items, stream); break;
+      case 3:
+      case 4: err = launch_fma<4>(tmk, tmv, P, n_items, stream); break;
+      default: err = launch_fma<8>(tmk, tmv, P, n_items, stream); break;
+    }
+  } else {
+    return PA_ERR_UNSUPPORTED;
+  }
+  if (err != cudaSuccess) return PA_ERR_CUDA;
+  if (n_combine > 0) {
+    CombineParams C{};
+    C.combine = combine;
+    C.work = work;
+    C.part_o = P.part_o;
+    C.part_lse = P.part_lse;
+    C.out = P.out;
+    C.status = P.status;
+    C.part_rows_cap = cap;
+    C.num_heads = c.num_heads;
+    C.group = P.group;
+    C.hv = hv;
+    if (launch_combine(C, n_combine, int(TR), stream) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+extern "C" pa_status pa_status_clear(void* workspace, void* stream) {
+  if (!workspace) return PA_ERR_INVALID_ARG;
+  return cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+extern "C" pa_status pa_status_read(const void* workspace, void* stream_, uint32_t* bits) {
+  if (!workspace) return PA_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (bits) *bits = v;
+  if (v & PA_STATUS_BIT_TIMEOUT) return PA_ERR_TIMEOUT;
+  if (v & PA_STATUS_BIT_BLOCK_INDEX) return PA_ERR_BLOCK_INDEX;
+  if (v & PA_STATUS_BIT_WORKSPACE) return PA_ERR_BUFFER_TOO_SMALL;
+  return PA_OK;
+}
+
+extern "C" const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported mode";
+    case PA_ERR_BUFFER_TOO_SMALL: return "buffer too small";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_BLOCK_INDEX: return "block table entry out of range";
+    case PA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}

@@ -1,0 +1,29 @@
+// Launch interface of the split-KV reduction kernel.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "pa.h"
+
+namespace pa {
+
+constexpr int kCombineThreads = 256;     // 8 warps, one row each
+constexpr int kCombineMaxSplits = 512;   // weights cached in shared memory
+
+struct CombineParams {
+  const int32_t* combine;
+  const int32_t* work;
+  const float* part_o;
+  const float* part_lse;
+  __half* out;
+  uint32_t* status;
+  int64_t part_rows_cap;
+  int num_heads, group, hv;
+};
+
+cudaError_t launch_combine(const CombineParams& C, int64_t n_combine, int tile_rows,
+                           cudaStream_t stream);
+
+}  // namespace pa

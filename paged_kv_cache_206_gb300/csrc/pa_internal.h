@@ -1,0 +1,56 @@
+// Host-side helpers shared by the planner and the launch code of libpa.so.
+#pragma once
+
+#include <cstdint>
+
+#include "pa.h"
+
+namespace pa {
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Checks of a pa_config against the operator's constraints (block_size % 16,
+// batch limit, GQA divisibility, head-size range, block_size <= 128 for head
+// sizes above 256 and for parallel decoding) and this library's own rules
+// (head sizes multiple of 16, supported mask types).
+pa_status validate_config(const pa_config* cfg);
+
+inline int64_t max_q(const pa_config& c) { return c.max_seqlen_q > 0 ? c.max_seqlen_q : 1; }
+
+// Tile height of a launch: every row of a (b, kv head) pair in one CTA when
+// the group is small enough for the CUDA-core kernel, else 64-row tiles.
+inline int64_t tile_rows(const pa_config& c) {
+  const int64_t g = c.num_heads / c.kv_heads;
+  const int64_t r = g * max_q(c);
+  return r <= PA_FMA_MAX_ROWS ? r : PA_TC_TILE_ROWS;
+}
+
+struct WorkspaceLayout {
+  size_t partial_o;    // byte offset of the fp32 [P, hv] partial outputs
+  size_t partial_lse;  // byte offset of the fp32 [P] log-sum-exps
+  size_t total;        // bytes
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WorkspaceLayout workspace_layout(int64_t partial_rows, int hv) {
+  WorkspaceLayout w;
+  w.partial_o = PA_STATUS_BYTES;
+  w.partial_lse = align256(w.partial_o + size_t(partial_rows) * size_t(hv) * 4);
+  w.total = align256(w.partial_lse + size_t(partial_rows) * 4);
+  return w;
+}
+
+// Partial rows that a workspace of `bytes` can hold for value head size hv.
+inline int64_t workspace_rows(size_t bytes, int hv) {
+  if (bytes < PA_STATUS_BYTES) return -1;
+  // largest P with workspace_layout(P, hv).total <= bytes
+  int64_t lo = 0, hi = int64_t((bytes - PA_STATUS_BYTES) / (size_t(hv) * 4 + 4)) + 1;
+  while (lo + 1 < hi) {
+    const int64_t mid = (lo + hi) / 2;
+    if (workspace_layout(mid, hv).total <= bytes) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+}  // namespace pa

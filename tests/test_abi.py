@@ -1,0 +1,95 @@
+"""The C ABI of libpa.so on a machine without a GPU: the library loads, exports
+every function that include/*.h declares, and rejects bad arguments on the host
+before it touches CUDA."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_206_gb300 as pa
+from paged_kv_cache_206_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return pa.load_library()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        names |= set(re.findall(r"\b(pa_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(pa.EXPORTS) <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", build_lib.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_library_does_not_link_the_driver(lib):
+    out = subprocess.run(["ldd", build_lib.LIB], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert pa.status_string(s) not in ("", "unknown status")
+    assert pa.status_string(99) == "unknown status"
+
+
+def _cfg(**kw):
+    base = dict(batch=1, num_heads=4, kv_heads=4, head_size_k=64, block_size=16, num_blocks=4,
+                max_blocks_per_seq=4, num_sms=1)
+    base.update(kw)
+    return pa.make_config(**base)
+
+
+def _fwd(lib, cfg, **ptrs):
+    """Call pa_forward with fake, aligned non-null addresses unless overridden."""
+    fake = ctypes.c_void_p(1 << 20)
+    args = dict(query=fake, key=fake, value=fake, bt=fake, ctx=fake, ql=None, mask=None,
+                slopes=None, work=fake, n_items=1, comb=None, n_comb=0, ws=fake, ws_bytes=256,
+                out=fake)
+    args.update(ptrs)
+    return lib.pa_forward(ctypes.byref(cfg), args["query"], args["key"], args["value"], args["bt"],
+                          args["ctx"], args["ql"], args["mask"], args["slopes"], args["work"],
+                          args["n_items"], args["comb"], args["n_comb"], args["ws"],
+                          args["ws_bytes"], args["out"], None)
+
+
+def test_forward_host_checks(lib):
+    c = _cfg()
+    fake = ctypes.c_void_p(1 << 20)
+    assert _fwd(lib, c, query=None) == pa.PA_ERR_INVALID_ARG
+    assert _fwd(lib, c, ws=None) == pa.PA_ERR_INVALID_ARG
+    assert _fwd(lib, c, mask=fake) == pa.PA_ERR_INVALID_ARG          # mask only with NORM_COMPRESS
+    assert _fwd(lib, _cfg(mask_type=5)) == pa.PA_ERR_INVALID_ARG     # NORM_COMPRESS needs a mask
+    assert _fwd(lib, _cfg(mask_type=2)) == pa.PA_ERR_INVALID_ARG     # ALIBI needs slopes
+    assert _fwd(lib, c, slopes=fake) == pa.PA_ERR_INVALID_ARG
+    assert _fwd(lib, _cfg(mask_type=4)) == pa.PA_ERR_UNSUPPORTED
+    assert _fwd(lib, _cfg(block_size=8)) == pa.PA_ERR_INVALID_ARG
+    assert _fwd(lib, c, key=ctypes.c_void_p((1 << 20) + 8)) == pa.PA_ERR_INVALID_ARG  # 16-B align
+    assert _fwd(lib, c, ws=ctypes.c_void_p((1 << 20) + 16)) == pa.PA_ERR_INVALID_ARG  # 256-B align
+    assert _fwd(lib, c, ws_bytes=255) == pa.PA_ERR_BUFFER_TOO_SMALL
+    assert _fwd(lib, c, n_comb=1, comb=None) == pa.PA_ERR_INVALID_ARG
+    assert _fwd(lib, c, n_items=-1) == pa.PA_ERR_INVALID_ARG
+    assert _fwd(lib, c, n_items=0, work=None) == pa.PA_OK              # nothing to do
+    assert lib.pa_status_clear(None, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_status_read(None, None, None) == pa.PA_ERR_INVALID_ARG
