@@ -1,0 +1,398 @@
+"""Benchmark: paged-attention effective KV HBM GB/s and query tokens/s.
+
+One step is one pass of the whole device path over one synthetic batch: the
+attention kernel over the planned work list plus the split-KV combine. The
+work list comes from pa_plan before the timed region (it is host code, timed
+separately as plan_us); the end-to-end number (`e2e`) puts the plan, the
+host->device copies of the step's inputs and the device->host read of the
+output inside its timed region.
+
+Default workload: GQA decode, B=64, H=32, Hk=8, hk=hv=128, block_size=128,
+context lengths uniform in [1, 4096], one query token per sequence, seed 0.
+Before every timed step a 512 MB buffer is written to flush the 129 MB L2, so
+every step reads the KV cache from HBM.
+
+`--impl reference` times the CPU oracle on this machine's cores instead, on a
+bounded sample of the same workload, and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn effective KV HBM GB/s (% of GB300 peak) and query tokens/s"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa_decode")
+    ap.add_argument("--chunk-blocks", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_206_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "pa.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    sources are unchanged since it was taken (else None)."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}.{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m_sha = re.search(r"^source_sha:\s*(\S+)", text, re.M)
+    m_b = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    if not (m_sha and m_b) or m_sha.group(1) != kernel_sources_sha():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle samples while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in (self.out or "").splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        # samples taken while the GPU was busy: the upper half of the clock readings
+        busy = sorted(sm)[len(sm) // 2:]
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload(name, rank, chunk):
+    from paged_kv_cache_206_gb300 import workloads as W
+    w = W.NAMED[name](seed=rank)
+    if chunk is not None:
+        w.chunk_blocks = chunk
+    return w
+
+
+def time_device(fn, steps, warmup, flush, stream):
+    """Per-step CUDA-event times (ms) of fn() on `stream`, L2 flushed before each step."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def cpu_baseline(w, max_seconds=20.0):
+    """The oracle on this machine's cores, on the whole batch or a prefix of it
+    sized to stay within about max_seconds."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    order = list(range(w.batch))
+    # estimate from one sequence, then take as many sequences as fit
+    t0 = time.perf_counter()
+    _, used = oracle.attention(w, subset=order[:1], threads=cores)
+    one = time.perf_counter() - t0
+    per_seq = max(one / max(1, min(used, 1)), 1e-4)
+    n = max(1, min(w.batch, int(max_seconds * min(cores, w.batch) / per_seq)))
+    sub = order[:n]
+    t0 = time.perf_counter()
+    _, used = oracle.attention(w, subset=sub, threads=cores)
+    dt = time.perf_counter() - t0
+    kv = int(w.context_lens[sub].astype(np.int64).sum()) * w.kv_heads * (w.head_size_k + w.head_size_v) * 2
+    return {"value": kv / dt / 1e9, "unit": UNIT, "cores": int(used), "kind": "oracle",
+            "seconds": dt,
+            "sample": f"{n} of {w.batch} sequences ({kv / 1e9:.3f} GB of KV), fp64 C oracle, "
+                      f"OpenMP over (sequence, kv head)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = workload(args.workload, 0, args.chunk_blocks)
+    cores = len(os.sched_getaffinity(0))
+    # bounded sample per step: the first n sequences, n sized for ~0.5 s per step
+    t0 = time.perf_counter()
+    oracle.attention(w, subset=[0], threads=cores)
+    one = max(time.perf_counter() - t0, 1e-4)
+    n = max(1, min(w.batch, int(0.5 * min(cores, w.batch) / one)))
+    sub = list(range(n))
+    kv = int(w.context_lens[sub].astype(np.int64).sum()) * w.kv_heads * (w.head_size_k + w.head_size_v) * 2
+    used = 1
+    for _ in range(args.warmup):
+        _, used = oracle.attention(w, subset=sub, threads=cores)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _, used = oracle.attention(w, subset=sub, threads=cores)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
+    value = kv / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "sample_sequences": n, "batch": w.batch},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": int(used), "kind": "oracle",
+                         "sample": f"{n} of {w.batch} sequences per step, fp64 C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import paged_kv_cache_206_gb300 as pa
+    from paged_kv_cache_206_gb300 import build_lib
+    if rank == 0 or world == 1:
+        build_lib.build()
+    if world > 1:
+        dist.barrier()
+
+    w = workload(args.workload, rank, args.chunk_blocks)
+    t0 = time.perf_counter()
+    db = pa.DeviceBatch(w, device=dev)
+    plan_reps = 50
+    t0 = time.perf_counter()
+    for _ in range(plan_reps):
+        pa.pa_plan(db.cfg, w.context_lens, None if np.all(w.q_seqlens == 1) else w.q_seqlens)
+    plan_us = (time.perf_counter() - t0) / plan_reps * 1e6
+
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    kv_bytes = w.kv_bytes()
+    qo_bytes = w.qo_bytes()
+    n_comb = db.plan.combine.shape[0]
+
+    def step():
+        db.forward(stream)
+
+    def decode_only():
+        pa.pa_forward(db.cfg, db.query, db.key_cache, db.value_cache, db.block_tables,
+                      db.context_lens, db.q_seqlens, db.mask, db.alibi_slopes, db.work, None,
+                      db.workspace, db.out, stream)
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) == 36:
+        gpu_id = "GPU-" + gpu_id
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as clk:
+        times = time_device(step, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    st, bits = db.status(stream)
+    if st != pa.PA_OK:
+        raise RuntimeError(f"kernel status {pa.status_string(st)} ({bits})")
+
+    # the dominant kernel alone: the same launch without the combine pass
+    dec_times = time_device(decode_only, max(50, args.steps // 4), 5, flush, stream)
+
+    # end to end through the C ABI with host buffers
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_query = pin(w.query)
+    h_bt = pin(w.block_tables)
+    h_ctx = pin(w.context_lens)
+    h_out = torch.empty(tuple(db.out.shape), dtype=torch.float16).pin_memory()
+    ql = None if np.all(w.q_seqlens == 1) else w.q_seqlens
+    n_items = db.plan.work.shape[0]
+    h_work = torch.empty((n_items, 8), dtype=torch.int32).pin_memory()
+    h_comb = torch.empty((max(n_comb, 1), 4), dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        plan = pa.pa_plan(db.cfg, h_ctx.numpy(), ql)
+        h_work.numpy()[:] = plan.work
+        if n_comb:
+            h_comb.numpy()[:n_comb] = plan.combine
+        db.query.copy_(h_query, non_blocking=True)
+        db.block_tables.copy_(h_bt, non_blocking=True)
+        db.context_lens.copy_(h_ctx, non_blocking=True)
+        db.work.copy_(h_work, non_blocking=True)
+        if n_comb:
+            db.combine.copy_(h_comb[:n_comb], non_blocking=True)
+        db.forward(stream)
+        h_out.copy_(db.out, non_blocking=True)
+        stream.synchronize()
+
+    h2d = (h_query.numel() * 2 + h_bt.numel() * 4 + h_ctx.numel() * 4 + h_work.numel() * 4 +
+           (n_comb * 4 * 4))
+    d2h = h_out.numel() * 2
+    for _ in range(5):
+        e2e_step()
+    e2e_t = []
+    for _ in range(args.e2e_steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_t.append(time.perf_counter() - t0)
+
+    ms = statistics.mean(times)
+    dec_ms = statistics.mean(dec_times)
+    e2e_s = statistics.mean(e2e_t)
+    if world > 1:
+        t = torch.tensor([ms, dec_ms, e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, dec_ms, e2e_s = t.tolist()
+        tot = torch.tensor([kv_bytes, qo_bytes, w.total_q], device=dev, dtype=torch.float64)
+        dist.all_reduce(tot)
+        kv_all, qo_all, q_all = tot.tolist()
+    else:
+        kv_all, qo_all, q_all = kv_bytes, qo_bytes, w.total_q
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = peaks()
+    value = kv_all / (ms * 1e-3) / 1e9
+    achieved = (kv_bytes + qo_bytes) / (dec_ms * 1e-3) / 1e9
+    traffic = ncu_traffic("fma_decode_kernel", args.workload)
+    base = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload, "batch": w.batch, "num_heads": w.num_heads,
+            "kv_heads": w.kv_heads, "head_size_k": w.head_size_k, "head_size_v": w.head_size_v,
+            "block_size": w.block_size, "q_per_seq": w.max_seqlen_q,
+            "mask_type": w.mask_type, "kv_bytes": kv_bytes, "qo_bytes": qo_bytes,
+            "items": n_items, "combines": n_comb, "chunk_blocks": db.cfg.chunk_blocks,
+            "l2": "512 MB buffer written before every step (outside the events)",
+            "plan_us": plan_us, "parallelism": f"replica x{world}" if world > 1 else "single",
+        },
+        "query_tokens_per_s": q_all / (ms * 1e-3),
+        "pct_of_nominal_8tbs": 100.0 * value / NOMINAL_HBM_GBS,
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+            "kernel": "fma_decode_kernel",
+            "bytes": "KV + Q + O per launch (algorithmic)", "kernel_ms": dec_ms,
+        },
+        "e2e": {"value": kv_all / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": args.steps * (1 + (1 if n_comb else 0)),
+        "clocks": clk.summary(),
+        "cpu_baseline": base,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

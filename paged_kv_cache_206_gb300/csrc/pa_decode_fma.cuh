@@ -114,13 +114,15 @@ __global__ void __launch_bounds__(128) fma_decode_kernel(const __grid_constant__
     }
     const int phys = __shfl_sync(FULL, bt_reg, rel - bt_base);
     if (lane == 0) {
-      int row;
       if (phys < 0 || phys >= P.num_blocks) {
+        // Never dereference a bad entry: flag it and complete the phase
+        // without a copy (the tile's scores are then meaningless, and the
+        // status word says so).
         set_status(P.status, PA_STATUS_BIT_BLOCK_INDEX);
-        row = P.num_blocks * bs;  // past the end of the map: the copy reads zeros
-      } else {
-        row = phys * bs + off;
+        mbar_arrive(&bars[buf]);
+        return;
       }
+      const int row = phys * bs + off;
       uint8_t* dst = my_bufs + buf * lay.buf_stride;
       mbar_arrive_expect_tx(&bars[buf], tile_bytes);
       for (int j = 0; j < nkbox; ++j)
@@ -235,9 +237,12 @@ __global__ void __launch_bounds__(128) fma_decode_kernel(const __grid_constant__
       if (P.mask_type == PA_MASK_ALIBI) {
         x += slope2[rr] * float(j - prow[rr]);
       } else if (P.mask_type == PA_MASK_NORM_COMPRESS) {
-        if (tok_ok && j > prefix)
-          x += __half2float(P.mask[int64_t(prow[rr] - sigma) * PA_COMPRESS_MASK_SIZE + (j - sigma)]) *
-               kLog2e;
+        if (tok_ok && j > prefix) {
+          // both indices lie in [0, 2048) for a consistent plan; clamp anyway
+          const int mr = min(max(prow[rr] - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
+          const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
+          x += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
+        }
       }
       x = tok_ok ? x : -INFINITY;
       float mt = x;

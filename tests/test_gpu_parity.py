@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Tolerance (fp16 outputs of O(1) magnitude, fp32 accumulation on the GPU,
+float64 in the oracle): max |gpu - oracle| <= 1e-2 and mean |gpu - oracle| <=
+1e-3 over every compared element. The work list is compared bit for bit with
+the oracle's planner in tests/test_plan.py; here the kernels run the list that
+pa_plan builds.
+
+Small cases run the oracle on every output element; they still span several
+16-token sub-tiles, several KV blocks per split, ragged last blocks and both
+split and unsplit items. The full-size workloads run on the GPU exactly as the
+benchmark launches them (automatic chunking for the device's SM count, 16-block
+chunks for the long-context MQA case) and compare sampled sequences.
+"""
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import paged_kv_cache_206_gb300 as pa
+from paged_kv_cache_206_gb300 import build_lib
+from paged_kv_cache_206_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 1e-2, 1e-3
+CORES = max(1, len(os.sched_getaffinity(0)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build_lib.build()
+    pa.load_library()
+
+
+def run_gpu(w, chunk_blocks=None):
+    db = pa.DeviceBatch(w, chunk_blocks=chunk_blocks)
+    out = db.forward()
+    st, bits = db.status()
+    assert st == pa.PA_OK, (pa.status_string(st), bits)
+    return out.float().cpu().numpy().astype(np.float64), db
+
+
+def compare(got, ref, rows=None):
+    if rows is not None:
+        got, ref = got[rows], ref[rows]
+    assert np.isfinite(got).all(), "non-finite GPU output"
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_ABS, f"max abs err {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"mean abs err {err.mean():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def full_parity(oracle_mod, w, chunk_blocks=None):
+    got, db = run_gpu(w, chunk_blocks)
+    ref, _ = oracle_mod.attention(w, threads=CORES)
+    return compare(got, ref), db
+
+
+# ---- small cases: every element against the oracle -------------------------
+
+CASES = {
+    "tiny_decode": lambda: W.tiny_decode(),
+    "gqa_small": lambda: W.gqa_decode(batch=8, max_len=1000, seed=1),
+    "spec_small": lambda: W.spec_decode(batch=4, max_len=2600, seed=2),
+    "alibi_small": lambda: W.alibi_decode(batch=6, max_len=700, seed=3),
+    "mqa8_hd512": lambda: W.make_workload("mqa8", context_lens=[700, 1500, 33], num_heads=8,
+                                          kv_heads=1, head_size_k=512, block_size=64, std=0.5,
+                                          seed=4),
+    "hk576_hv512": lambda: W.make_workload("mla", context_lens=[300, 77], num_heads=4,
+                                           kv_heads=1, head_size_k=576, head_size_v=512,
+                                           block_size=64, seed=5),
+    "hk96": lambda: W.make_workload("hk96", context_lens=[129, 40, 300], num_heads=6,
+                                    kv_heads=2, head_size_k=96, block_size=32, seed=6),
+    "hk80_hv48": lambda: W.make_workload("hk80", context_lens=[50, 211], num_heads=2,
+                                         kv_heads=2, head_size_k=80, head_size_v=48,
+                                         block_size=16, seed=7),
+    "hk256_g8": lambda: W.make_workload("g8", context_lens=[1, 2, 15, 16, 17, 255, 256, 257],
+                                        num_heads=16, kv_heads=2, head_size_k=256,
+                                        block_size=128, seed=8),
+    "g2_q3_mask": lambda: W.make_workload("g2q3", context_lens=[3, 4, 20, 129, 2047, 2048, 2049,
+                                                               3000],
+                                          q_seqlens=3, num_heads=4, kv_heads=2,
+                                          head_size_k=64, block_size=32,
+                                          mask_type=W.MASK_NORM_COMPRESS, seed=9),
+    "q_ragged_mask": lambda: W.make_workload("qr", context_lens=[5, 64, 300, 2100, 9],
+                                             q_seqlens=[1, 8, 3, 5, 8], num_heads=1,
+                                             kv_heads=1, head_size_k=128, block_size=64,
+                                             mask_type=W.MASK_NORM_COMPRESS, seed=10),
+    "mask_60000": lambda: W.make_workload("m6", context_lens=[40, 2200], q_seqlens=4,
+                                          num_heads=2, kv_heads=2, head_size_k=128,
+                                          block_size=128, mask_type=W.MASK_NORM_COMPRESS,
+                                          mask_fill=-60000.0, seed=11),
+    "alibi_q2_gqa": lambda: W.make_workload("aq", context_lens=[9, 300, 1000], q_seqlens=2,
+                                            num_heads=8, kv_heads=2, head_size_k=128,
+                                            block_size=16, mask_type=W.MASK_ALIBI, seed=12),
+    "bs16_long": lambda: W.make_workload("bs16", context_lens=[4000, 1, 17], num_heads=4,
+                                         kv_heads=4, head_size_k=128, block_size=16, seed=13),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_small_parity(oracle_mod, name):
+    full_parity(oracle_mod, CASES[name]())
+
+
+@pytest.mark.parametrize("chunk", [1, 2, 5, 1000])
+def test_chunking_does_not_change_the_result(oracle_mod, chunk):
+    w = W.gqa_decode(batch=6, max_len=1500, seed=20)
+    (mx, mean), db = full_parity(oracle_mod, w, chunk_blocks=chunk)
+    if chunk == 1:
+        assert db.plan.combine.shape[0] > 0
+    if chunk == 1000:
+        assert db.plan.combine.shape[0] == 0
+
+
+def test_split_and_unsplit_agree(oracle_mod):
+    w = W.spec_decode(batch=3, max_len=3000, seed=21)
+    a, _ = run_gpu(w, chunk_blocks=1)
+    b, _ = run_gpu(w, chunk_blocks=100)
+    compare(a, b)
+
+
+def test_repeat_runs_are_identical():
+    w = W.gqa_decode(batch=8, max_len=2000, seed=22)
+    db = pa.DeviceBatch(w)
+    a = db.forward().clone()
+    b = db.forward().clone()
+    assert torch.equal(a, b)
+
+
+def test_block_index_out_of_range_is_reported():
+    """A table entry outside [0, num_blocks) is flagged by the kernel's own bounds
+    check and never dereferenced; the other sequences are unaffected."""
+    w = W.gqa_decode(batch=4, max_len=600, seed=23)
+    good = pa.DeviceBatch(w, chunk_blocks=1000)
+    ref = good.forward().clone()
+    w.block_tables[2, 0] = w.num_blocks + 5
+    bad = pa.DeviceBatch(w, chunk_blocks=1000)
+    out = bad.forward()
+    st, bits = bad.status()
+    assert st == pa.PA_ERR_BLOCK_INDEX and bits & 1
+    keep = np.ones(w.total_q, bool)
+    keep[2] = False
+    assert torch.equal(out[torch.from_numpy(keep).cuda()], ref[torch.from_numpy(keep).cuda()])
+    pa.pa_status_clear(bad.workspace)
+    assert bad.status()[0] == pa.PA_OK
+
+
+def test_tensor_core_tiles_not_yet_supported():
+    """Row tiles above 8 rows go to the tensor-core kernel."""
+    w = W.make_workload("wide", context_lens=[100], num_heads=16, kv_heads=1, head_size_k=128,
+                        block_size=16)
+    with pytest.raises(pa.PaError) as e:
+        run_gpu(w)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
+
+
+# ---- full-size workloads: sampled sequences ------------------------------------
+
+def sample_rows(w, k, seed):
+    rng = np.random.default_rng(seed)
+    L = w.context_lens
+    pick = {int(np.argmax(L)), int(np.argmin(L))}
+    pick |= set(rng.choice(w.batch, size=min(k, w.batch), replace=False).tolist())
+    pick = sorted(pick)
+    qs = np.concatenate([[0], np.cumsum(w.q_seqlens)])
+    rows = np.concatenate([np.arange(qs[b], qs[b + 1]) for b in pick])
+    return pick, rows
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["gqa_decode", "spec_decode", "alibi_decode"])
+def test_full_size_sampled(oracle_mod, name):
+    w = W.NAMED[name]()
+    got, db = run_gpu(w)
+    pick, rows = sample_rows(w, 6, 99)
+    ref, _ = oracle_mod.attention(w, subset=pick, threads=CORES)
+    compare(got, ref, rows)
+    # every output row is finite (NaN-poisoned tail slots and spare blocks never read)
+    assert np.isfinite(got).all()
