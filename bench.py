@@ -84,6 +84,16 @@ def ncu_traffic(kernel: str, workload: str):
     return float(m_b.group(1))
 
 
+def dominant_kernel(cfg):
+    """The attention kernel pa_forward picks for this configuration."""
+    rows = (cfg.num_heads // cfg.kv_heads) * max(1, cfg.max_seqlen_q)
+    if rows > 8:
+        return "tc_decode_kernel"
+    mma = (cfg.head_size_k == cfg.head_size_v and cfg.head_size_k in (64, 128, 256, 512)) or \
+        (cfg.head_size_k, cfg.head_size_v) == (576, 512)
+    return "mma_decode_kernel" if rows >= 2 and mma else "fma_decode_kernel"
+
+
 class ClockSampler:
     """nvidia-smi clock and throttle samples while the timed region runs."""
 
@@ -321,7 +331,7 @@ def main():
     h2d = (h_query.numel() * 2 + h_bt.numel() * 4 + h_ctx.numel() * 4 + h_work.numel() * 4 +
            (n_comb * 4 * 4))
     d2h = h_out.numel() * 2
-    for _ in range(5):
+    for _ in range(min(5, args.e2e_steps)):
         e2e_step()
     e2e_t = []
     for _ in range(args.e2e_steps):
@@ -333,7 +343,7 @@ def main():
 
     ms = statistics.mean(times)
     dec_ms = statistics.mean(dec_times)
-    e2e_s = statistics.mean(e2e_t)
+    e2e_s = statistics.mean(e2e_t) if e2e_t else float("nan")
     if world > 1:
         t = torch.tensor([ms, dec_ms, e2e_s], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -351,7 +361,8 @@ def main():
     peak, peak_kind = peaks()
     value = kv_all / (ms * 1e-3) / 1e9
     achieved = (kv_bytes + qo_bytes) / (dec_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("fma_decode_kernel", args.workload)
+    kernel = dominant_kernel(db.cfg)
+    traffic = ncu_traffic(kernel, args.workload)
     base = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w)
     line = {
         "metric": METRIC,
@@ -380,11 +391,12 @@ def main():
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-            "kernel": "fma_decode_kernel",
+            "kernel": kernel,
             "bytes": "KV + Q + O per launch (algorithmic)", "kernel_ms": dec_ms,
         },
-        "e2e": {"value": kv_all / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3},
+        "e2e": None if not e2e_t else {
+            "value": kv_all / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3},
         "gpu_launches": args.steps * (1 + (1 if n_comb else 0)),
         "clocks": clk.summary(),
         "cpu_baseline": base,

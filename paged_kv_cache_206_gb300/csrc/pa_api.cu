@@ -10,6 +10,8 @@
 
 #include "pa.h"
 #include "pa_combine.cuh"
+#include "pa_decode_mma.cuh"
+#include "pa_decode_tc.cuh"
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -41,12 +43,13 @@ struct BoxGeom {
   CUtensorMapSwizzle swizzle;
 };
 
-// Widest box (<= 128 bytes) that divides the head size, with the matching
-// swizzle so that reads of one 16-byte chunk column across rows hit distinct
+// TMA box width and swizzle: 64-element (128-byte) boxes with the 128-byte
+// swizzle when both head sizes are multiples of 64, else 16-element boxes
+// with the 32-byte swizzle (16 divides every valid head size). Either way a
+// column of 16-byte chunks read across consecutive token rows hits distinct
 // shared-memory banks.
-BoxGeom box_geom(int head_size) {
-  if (head_size % 64 == 0) return {64, 7u, CU_TENSOR_MAP_SWIZZLE_128B};
-  if (head_size % 32 == 0) return {32, 3u, CU_TENSOR_MAP_SWIZZLE_64B};
+BoxGeom box_geom(bool wide) {
+  if (wide) return {64, 7u, CU_TENSOR_MAP_SWIZZLE_128B};
   return {16, 1u, CU_TENSOR_MAP_SWIZZLE_32B};
 }
 
@@ -129,15 +132,14 @@ extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const v
 
   cudaError_t err;
   if (TR <= PA_FMA_MAX_ROWS) {
-    const BoxGeom kg = box_geom(hk), vg = box_geom(hv);
-    P.kbw = kg.width;
-    P.vbw = vg.width;
-    P.kswz = kg.swz_mask;
-    P.vswz = vg.swz_mask;
+    const bool wide = (hk % 64 == 0) && (hv % 64 == 0);
+    const BoxGeom kg = box_geom(wide), vg = box_geom(wide);
     CUtensorMap tmk, tmv;
     if (!cache_map(&tmk, key_cache, c, hk, 16, kg) || !cache_map(&tmv, value_cache, c, hv, 16, vg))
       return PA_ERR_CUDA;
-    switch (TR) {
+    if (TR >= 2 && mma_supported(hk, hv)) {
+      err = launch_mma(tmk, tmv, P, n_items, stream);
+    } else switch (TR) {
       case 1: err = launch_fma<1>(tmk, tmv, P, n_items, stream); break;
       case 2: err = launch_fma<2>(tmk, tmv, P, n_items, stream); break;
       case 3:
@@ -145,7 +147,14 @@ extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const v
       default: err = launch_fma<8>(tmk, tmv, P, n_items, stream); break;
     }
   } else {
-    return PA_ERR_UNSUPPORTED;
+    // 64-row tiles on the tcgen05 kernel: boxes of min(block_size, 128) tokens
+    if (!tc_supported(hk, hv)) return PA_ERR_UNSUPPORTED;
+    const BoxGeom g = box_geom(true);
+    const int rows = c.block_size < 128 ? c.block_size : 128;
+    CUtensorMap tmk, tmv;
+    if (!cache_map(&tmk, key_cache, c, hk, rows, g) || !cache_map(&tmv, value_cache, c, hv, rows, g))
+      return PA_ERR_CUDA;
+    err = launch_tc(tmk, tmv, P, n_items, stream);
   }
   if (err != cudaSuccess) return PA_ERR_CUDA;
   if (n_combine > 0) {

@@ -5,12 +5,16 @@
 //   out = sum_s exp(lse_s - M) * O_s / sum_s exp(lse_s - M),  M = max_s lse_s.
 // One warp merges one row; a CTA takes kCombineRows rows of one combine entry.
 #include "pa_combine.cuh"
+#include "pa_device.cuh"
 
 namespace pa {
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams C) {
   __shared__ float wts[kCombineThreads / 32][kCombineMaxSplits];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // Launched as a programmatic dependent of the attention kernel: wait until
+  // that grid has finished and its partial results are visible.
+  grid_dependency_wait();
   const int32_t* e = C.combine + int64_t(blockIdx.x) * PA_COMBINE_INTS;
   const int kvh = e[1], first = e[2], S = e[3];
   const int32_t* item = C.work + int64_t(first) * PA_WORK_INTS;
@@ -59,9 +63,18 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 
 cudaError_t launch_combine(const CombineParams& C, int64_t n_combine, int tile_rows,
                            cudaStream_t stream) {
-  dim3 grid(unsigned(n_combine), unsigned((tile_rows + kCombineThreads / 32 - 1) / (kCombineThreads / 32)));
-  combine_kernel<<<grid, kCombineThreads, 0, stream>>>(C);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(n_combine),
+                     unsigned((tile_rows + kCombineThreads / 32 - 1) / (kCombineThreads / 32)));
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, C);
 }
 
 }  // namespace pa

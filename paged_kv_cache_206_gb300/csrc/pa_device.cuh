@@ -93,26 +93,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Packed fp32 fused multiply-add on register pairs: d = a * b + c, lane-wise.
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t ra, rb, rc, rd;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
-  return d;
-}
+// Packed fp32 fused multiply-add / multiply on register pairs (FFMA2/FMUL2 of
+// sm_100 and later): d = a * b + c, lane-wise.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  uint64_t ra, rb, rd;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
-  return d;
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 __device__ __forceinline__ float2 h2f2(uint32_t h) {
@@ -124,6 +112,16 @@ __device__ __forceinline__ float2 h2f2(uint32_t h) {
 // swizzle: bits [4, 4+w) of the offset are XOR-ed with bits [7, 7+w).
 __device__ __forceinline__ uint32_t swz(uint32_t off, uint32_t mask) {
   return off ^ (((off >> 7) & mask) << 4);
+}
+
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled (it still waits in grid_dependency_wait until this grid has
+// completed and its memory operations are visible).
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
@@ -150,9 +148,6 @@ struct FwdParams {
   int num_heads, kv_heads, group, hk, hv, block_size, max_blocks_per_seq, num_blocks;
   int mask_type;
   float scale_log2;  // scale * log2(e)
-  // K/V box geometry: box width (elements) per TMA copy and the swizzle mask
-  int kbw, vbw;
-  uint32_t kswz, vswz;
 };
 
 }  // namespace pa

@@ -151,9 +151,49 @@ def test_block_index_out_of_range_is_reported():
     assert bad.status()[0] == pa.PA_OK
 
 
-def test_tensor_core_tiles_not_yet_supported():
-    """Row tiles above 8 rows go to the tensor-core kernel."""
-    w = W.make_workload("wide", context_lens=[100], num_heads=16, kv_heads=1, head_size_k=128,
+# ---- 64-row tiles (tcgen05 kernel) -------------------------------------------
+
+TC_CASES = {
+    # 16 rows, bs=16: a 128-token tile gathers 8 blocks; ragged last tile
+    "tc_r16_bs16": lambda: W.make_workload("r16", context_lens=[100, 300, 17, 129], num_heads=16,
+                                           kv_heads=1, head_size_k=128, block_size=16, seed=30),
+    # the long-context MQA shape, shortened: 64 heads on one kv head of 512 dims
+    "tc_mqa_hd512": lambda: W.make_workload("mqa", context_lens=[2085, 700, 128, 1], num_heads=64,
+                                            kv_heads=1, head_size_k=512, block_size=128,
+                                            std=0.5, seed=31, chunk_blocks=4),
+    # 64 rows = GQA 16 x 4 speculative tokens, compressed causal mask past 2048
+    "tc_spec_mask": lambda: W.make_workload("tcm", context_lens=[2200, 64, 700], q_seqlens=4,
+                                            num_heads=32, kv_heads=2, head_size_k=128,
+                                            block_size=64, mask_type=W.MASK_NORM_COMPRESS, seed=32),
+    # ALiBi with 24 rows on hk=256
+    "tc_alibi_hd256": lambda: W.make_workload("tca", context_lens=[300, 1000], num_heads=24,
+                                              kv_heads=1, head_size_k=256, block_size=32,
+                                              mask_type=W.MASK_ALIBI, seed=33),
+    # 128 rows per (b, kv head): two row tiles, ragged q
+    "tc_two_tiles": lambda: W.make_workload("tc2", context_lens=[500, 130], q_seqlens=[4, 3],
+                                            num_heads=32, kv_heads=1, head_size_k=128,
+                                            block_size=128, mask_type=W.MASK_NORM_COMPRESS, seed=34),
+    # block_size 256: a tile is half a block
+    "tc_bs256": lambda: W.make_workload("tc256", context_lens=[600, 256, 257], num_heads=16,
+                                        kv_heads=1, head_size_k=128, block_size=256, seed=35),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TC_CASES))
+def test_tensor_core_parity(oracle_mod, name):
+    full_parity(oracle_mod, TC_CASES[name]())
+
+
+def test_tensor_core_split_and_unsplit_agree(oracle_mod):
+    w = TC_CASES["tc_mqa_hd512"]()
+    a, _ = run_gpu(w, chunk_blocks=1)
+    b, _ = run_gpu(w, chunk_blocks=100)
+    compare(a, b)
+
+
+def test_tensor_core_unsupported_head_size():
+    """64-row tiles are built for hk = hv in {128, 256, 512}."""
+    w = W.make_workload("wide64", context_lens=[100], num_heads=16, kv_heads=1, head_size_k=64,
                         block_size=16)
     with pytest.raises(pa.PaError) as e:
         run_gpu(w)
@@ -174,11 +214,11 @@ def sample_rows(w, k, seed):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["gqa_decode", "spec_decode", "alibi_decode"])
+@pytest.mark.parametrize("name", ["gqa_decode", "spec_decode", "alibi_decode", "mqa_split"])
 def test_full_size_sampled(oracle_mod, name):
     w = W.NAMED[name]()
     got, db = run_gpu(w)
-    pick, rows = sample_rows(w, 6, 99)
+    pick, rows = sample_rows(w, 2 if name == "mqa_split" else 6, 99)
     ref, _ = oracle_mod.attention(w, subset=pick, threads=CORES)
     compare(got, ref, rows)
     # every output row is finite (NaN-poisoned tail slots and spare blocks never read)
