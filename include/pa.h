@@ -219,6 +219,39 @@ pa_status pa_forward(const pa_config* cfg, const void* query, const void* key_ca
                      const int32_t* combine, int64_t n_combine, void* workspace,
                      size_t workspace_bytes, void* out, void* stream);
 
+/*
+ * pa_forward_noalloc -- pa_forward without a caller-provided workspace.
+ *
+ * The reference pages have no counterpart to this call; it exists for callers
+ * that cannot allocate device memory: code whose device memory is owned by a
+ * pool or an inference runtime that forbids ad-hoc allocations while serving,
+ * and latency-critical loops that cannot afford the implicit synchronisation a
+ * cudaMalloc/cudaFree may cause. It allocates nothing: the workspace is a fixed
+ * device array of PA_NOALLOC_SCRATCH_BYTES inside libpa.so, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * Arguments are those of pa_forward, except:
+ * workspace_bytes  the size pa_plan reported for this batch; more than
+ *                  PA_NOALLOC_SCRATCH_BYTES returns PA_ERR_BUFFER_TOO_SMALL
+ *                  before anything is enqueued.
+ * status           device uint32 or NULL; when non-NULL it receives, on the
+ *                  stream, the status word of this call (PA_STATUS_BIT_* flags).
+ *
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture. Each call zeroes the array's status word on the
+ * stream before launching. All calls on a device share the one array, so calls
+ * whose work overlaps on the GPU (other streams, other host threads) race.
+ * Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+pa_status pa_forward_noalloc(const pa_config* cfg, const void* query, const void* key_cache,
+                             const void* value_cache, const int32_t* block_tables,
+                             const int32_t* context_lens, const int32_t* q_seqlens,
+                             const void* mask, const float* alibi_slopes, const int32_t* work,
+                             int64_t n_items, const int32_t* combine, int64_t n_combine,
+                             size_t workspace_bytes, uint32_t* status, void* out, void* stream);
+
 /* Zero the status word of a workspace (enqueued on stream). */
 pa_status pa_status_clear(void* workspace, void* stream);
 

@@ -35,7 +35,11 @@ PA_COMBINE_INTS = 4
 PA_STATUS_BYTES = 256
 
 # Every symbol include/pa.h declares.
-EXPORTS = ("pa_plan", "pa_forward", "pa_status_clear", "pa_status_read", "pa_status_string")
+EXPORTS = ("pa_plan", "pa_forward", "pa_forward_noalloc", "pa_status_clear", "pa_status_read",
+           "pa_status_string")
+
+# Size of the device array pa_forward_noalloc uses as its workspace.
+PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class PaError(RuntimeError):
@@ -83,6 +87,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.pa_plan.argtypes = [cfgp, P, P, P, i64, P, P, i64, P, P]
     lib.pa_forward.restype = ctypes.c_int
     lib.pa_forward.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, i64, P, i64, P, sz, P, P]
+    lib.pa_forward_noalloc.restype = ctypes.c_int
+    lib.pa_forward_noalloc.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, i64, P, i64, sz, P, P, P]
     lib.pa_status_clear.restype = ctypes.c_int
     lib.pa_status_clear.argtypes = [P, P]
     lib.pa_status_read.restype = ctypes.c_int
@@ -174,6 +180,25 @@ def pa_forward(cfg: pa_config, query, key_cache, value_cache, block_tables, cont
                         workspace.numel() * workspace.element_size(), _tptr(out),
                         _stream_handle(stream))
     _check(st, "pa_forward")
+
+
+def pa_forward_noalloc(cfg: pa_config, query, key_cache, value_cache, block_tables,
+                       context_lens, q_seqlens, mask, alibi_slopes, work, combine,
+                       workspace_bytes: int, status, out, stream=None) -> None:
+    """Enqueue attention without a workspace argument (pa_forward_noalloc): for
+    callers that cannot allocate device memory, the library's own fixed device
+    array serves as the workspace. ``workspace_bytes`` is what pa_plan
+    reported; ``status`` is a CUDA uint32/int32 tensor of one element, or None."""
+    lib = load_library()
+    n_items = 0 if work is None else work.shape[0]
+    n_comb = 0 if combine is None else combine.shape[0]
+    st = lib.pa_forward_noalloc(ctypes.byref(cfg), _tptr(query), _tptr(key_cache),
+                                _tptr(value_cache), _tptr(block_tables), _tptr(context_lens),
+                                _tptr(q_seqlens), _tptr(mask), _tptr(alibi_slopes), _tptr(work),
+                                n_items, _tptr(combine) if n_comb else None, n_comb,
+                                int(workspace_bytes), _tptr(status), _tptr(out),
+                                _stream_handle(stream))
+    _check(st, "pa_forward_noalloc")
 
 
 def pa_status_clear(workspace, stream=None) -> None:
