@@ -69,6 +69,24 @@ bool cache_map(CUtensorMap* m, const void* base, const pa_config& c, int hs, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same cache as a 3-D tensor for the tcgen05 kernel: dims (64 elements of
+// a head-dim block, token rows, head-dim blocks of all kv heads), strides
+// (row stride, 128 bytes); a box is box_rows tokens x `halves` blocks of 64
+// dims, each landing as its own [box_rows][128 B] swizzled tile.
+bool cache_map_3d(CUtensorMap* m, const void* base, const pa_config& c, int hs, int box_rows,
+                  int halves) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, cuuint64_t(c.num_blocks) * c.block_size,
+                        cuuint64_t(c.kv_heads) * (hs / 64)};
+  cuuint64_t strides[2] = {cuuint64_t(c.kv_heads) * hs * 2, 128};
+  cuuint32_t box[3] = {64, cuuint32_t(box_rows), cuuint32_t(halves)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
@@ -147,12 +165,13 @@ extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const v
       default: err = launch_fma<8>(tmk, tmv, P, n_items, stream); break;
     }
   } else {
-    // 64-row tiles on the tcgen05 kernel: boxes of min(block_size, 128) tokens
+    // 64-row tiles on the tcgen05 kernel: boxes of min(block_size, 64) tokens
     if (!tc_supported(hk, hv)) return PA_ERR_UNSUPPORTED;
-    const BoxGeom g = box_geom(true);
-    const int rows = c.block_size < 128 ? c.block_size : 128;
+    const int rows = c.block_size < 64 ? c.block_size : 64;
+    const int halves = rows == 64 ? 2 : 1;
     CUtensorMap tmk, tmv;
-    if (!cache_map(&tmk, key_cache, c, hk, rows, g) || !cache_map(&tmv, value_cache, c, hv, rows, g))
+    if (!cache_map_3d(&tmk, key_cache, c, hk, rows, halves) ||
+        !cache_map_3d(&tmv, value_cache, c, hv, rows, halves))
       return PA_ERR_CUDA;
     err = launch_tc(tmk, tmv, P, n_items, stream);
   }

@@ -4,23 +4,55 @@
 // QK^T and PV real dense tiles. PagedAttentionOperation semantics (block
 // tables, context lengths, mask/bias); split/merge as in the metadata page.
 //
-// One CTA per work item, 6 warps:
+// One CTA per work item, 10 warps:
 //   warp 0     TMA producer: 128-token x 64-dim boxes (16 KB, 128-byte swizzle)
 //              of K then V of each 128-token tile into a ring of 8 slots.
 //   warp 1     allocates TMEM; one thread issues the MMAs:
 //                S^T[128 tok x 64 rows]  = K . Q^T           (A, B K-major)
 //                O^T[hv x 64 rows]      += V^T . P^T         (A, B MN-major)
 //              with S^T and O^T accumulated in TMEM (fp32).
-//   warps 2-5  softmax: thread = token (TMEM lane), its 64 scores in registers;
-//              row max and row sum across the 128 tokens by a butterfly
-//              reduce-scatter in each warp plus a 4-warp exchange in shared
-//              memory; P^T (fp16) written to shared memory in the MN-major
-//              swizzled layout the PV MMA reads; O^T rescaled in TMEM only when
-//              a row's reference max must grow by more than 2^8 (exact: the
-//              final normalisation uses the same reference); then the epilogue
-//              (thread = output dim) reads O^T from TMEM and writes the rows.
+//   warps 2-9  softmax: two warps per TMEM lane quarter; thread = token (TMEM
+//              lane) and one half (32) of the 64 rows, its scores in registers.
+//              Probabilities are taken against a per-row reference max that is
+//              recomputed exactly (warp max + 4-quarter exchange) only when some
+//              score exceeds it by more than 2^8 -- in practice the first tile;
+//              O^T and the sums are rescaled then (exact: the final
+//              normalisation uses the same reference). Row sums accumulate per
+//              token and are reduced across tokens once, at the end. P^T (fp16)
+//              goes to shared memory in the MN-major swizzled layout the PV MMA
+//              reads. Epilogue: thread = output dim, O^T / l from TMEM to out.
 // Every wait is bounded; on a timeout the CTA records PA_STATUS_BIT_TIMEOUT,
 // lets its copies land, frees its TMEM and exits.
+// Split-KV paged decode on the 5th-generation tensor cores (tcgen05 + TMEM) for
+// 64-row query tiles: a wide GQA/MQA group (e.g. 64 query heads sharing one kv
+// head of 512 dims, the shape of SparseAttnSharedkvMetadata's operator) makes
+// QK^T and PV real dense tiles. PagedAttentionOperation semantics (block
+// tables, context lengths, mask/bias); split/merge as in the metadata page.
+//
+// The KV range of a work item is cut into 64-token tiles. One CTA per item,
+// 12 warps:
+//   warp 0     K producer: 3-D TMA boxes of 64 tokens x 128 dims (16 KB, two
+//              128-byte-swizzled 64-dim halves) into a 3-slot K ring.
+//   warp 10    V producer: the same for V into a 5-slot V ring.
+//   warp 1     allocates TMEM; one thread issues S^T[64 tok x 64 rows] = K . Q^T
+//              (M=64; A, B K-major) into one of two S^T buffers in TMEM, up to
+//              two tiles ahead of the softmax.
+//   warp 11    one thread issues O^T[hv x 64 rows] += V^T . P^T (M=128; A, B
+//              MN-major) as soon as a tile's P^T is ready; O^T stays in TMEM.
+//   warps 2-9  softmax: two warps per TMEM lane quarter; with M=64 a quarter
+//              holds 16 tokens (lanes 0-15), and each warp of the pair takes 32
+//              of the 64 rows. Probabilities are taken against a per-row
+//              reference max that is recomputed exactly (warp max + 4-quarter
+//              exchange) only when some score exceeds it by more than 2^8 -- in
+//              practice the first tile; O^T and the sums are rescaled then
+//              (exact: the final normalisation uses the same reference). Row
+//              sums accumulate per token and are reduced across tokens once, at
+//              the end. P^T (fp16, double-buffered) goes to shared memory in the
+//              MN-major swizzled layout the PV MMA reads. Epilogue: thread =
+//              output dim, O^T / l from TMEM to the output or the split partials.
+// Separate rings and issuers keep K streaming into QK while a tile's V waits
+// for its softmax. Every wait is bounded; on a timeout the CTA records
+// PA_STATUS_BIT_TIMEOUT, lets its copies land, frees its TMEM and exits.
 #pragma once
 
 #include "pa_device.cuh"
@@ -29,10 +61,12 @@
 namespace pa {
 
 constexpr int kTcRows = PA_TC_TILE_ROWS;  // N of both MMAs (query rows, padded)
-constexpr int kTcTok = 128;               // M of QK^T: tokens per tile
-constexpr int kTcSlots = 8;               // ring of 16 KB boxes
-constexpr uint32_t kTcSlotBytes = kTcTok * 128;  // 128 tokens x 64 dims x 2 B
-constexpr int kTcThreads = 192;
+constexpr int kTcTok = 64;                // tokens per tile (M of QK^T)
+constexpr int kTcKSlots = 3;              // K ring of 16 KB boxes
+constexpr int kTcVSlots = 5;              // V ring of 16 KB boxes
+constexpr uint32_t kTcHalfBytes = kTcTok * 128;      // 64 tokens x 64 dims x 2 B
+constexpr uint32_t kTcSlotBytes = 2 * kTcHalfBytes;  // 64 tokens x 128 dims
+constexpr int kTcThreads = 384;  // 2 producers, 2 MMA issuers, 8 softmax warps
 constexpr float kTcRescaleThreshold = 8.f;  // log2 units
 
 struct TcLayout {
@@ -41,19 +75,19 @@ struct TcLayout {
 
 __host__ __device__ inline TcLayout tc_layout(int hk) {
   TcLayout L;
-  L.q_off = 0;                                          // [hk/64][64 rows][128 B]
-  L.p_off = L.q_off + uint32_t(hk / 64) * kTcRows * 128;  // [128 tok][64 rows] fp16
-  L.ring_off = L.p_off + kTcTok * 128;                  // kTcSlots x 16 KB
-  L.red_off = L.ring_off + kTcSlots * kTcSlotBytes;     // [4 warps][64] fp32 exchange
-  L.rows_off = L.red_off + 4 * kTcRows * 4;             // per-row constants
-  L.bars_off = L.rows_off + 6 * kTcRows * 4;            // mbarriers
-  L.tmem_slot_off = L.bars_off + (2 * kTcSlots + 4) * 8;
+  L.q_off = 0;                                            // [hk/64][64 rows][128 B]
+  L.p_off = L.q_off + uint32_t(hk / 64) * kTcRows * 128;  // 2 x [64 tok][64 rows] fp16
+  L.ring_off = L.p_off + 2 * kTcTok * 128;                // K ring, then V ring
+  L.red_off = L.ring_off + (kTcKSlots + kTcVSlots) * kTcSlotBytes;  // [4][64] fp32 exchange
+  L.rows_off = L.red_off + 4 * kTcRows * 4;               // per-row constants
+  L.bars_off = L.rows_off + 6 * kTcRows * 4;              // mbarriers
+  L.tmem_slot_off = L.bars_off + (2 * (kTcKSlots + kTcVSlots) + 12) * 8;
   L.bytes = L.tmem_slot_off + 16 + 1024;
   return L;
 }
 
-// Head-size pairs the tcgen05 kernel is instantiated for (K boxes are consumed
-// one 64-dim box at a time, V boxes in adjacent pairs of 128 dims).
+// Head-size pairs the tcgen05 kernel is instantiated for (K and V move in
+// 128-dim halves of a 16 KB box).
 inline bool tc_supported(int hk, int hv) {
   return hk == hv && (hk == 128 || hk == 256 || hk == 512);
 }
@@ -141,22 +175,29 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Named barrier among the 128 softmax threads (warps 2-5).
+// Named barrier among the 256 softmax threads (warps 2-9).
 __device__ __forceinline__ void softmax_bar() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
-// The same barrier, returning the OR of `pred` over the 128 threads: every
+// The same barrier, returning the OR of `pred` over the 256 threads: every
 // softmax thread takes the same continue/abort decision.
 __device__ __forceinline__ bool softmax_bar_or(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.or.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      " bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
       : "=r"(r)
       : "r"(uint32_t(pred))
       : "memory");
   return r != 0;
+}
+
+// Maximum over the warp (redux.sync, float form of sm_100 and later).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 // Lane 0 waits; the whole warp gets its verdict.
@@ -166,21 +207,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int la
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// Butterfly reduce-scatter of v[64] (one value per row) across the warp:
-// afterwards lane l holds the reduction of rows 2l and 2l+1 in v[0], v[1].
-template <bool MAX>
-__device__ __forceinline__ void reduce_scatter64(float (&v)[64], int lane) {
+// Butterfly reduce-scatter (sum) of v[32] across the warp: afterwards lane l
+// holds, in v[0], the sum over the 32 lanes of element l.
+__device__ __forceinline__ void reduce_scatter32_add(float (&v)[32], int lane) {
 #pragma unroll
   for (int lvl = 0; lvl < 5; ++lvl) {
     const int off = 16 >> lvl;
-    const int half = 32 >> lvl;  // values kept after this level
+    const int half = 16 >> lvl;  // values kept after this level
     const bool upper = lane & off;
 #pragma unroll
     for (int i = 0; i < half; ++i) {
       const float send = upper ? v[i] : v[i + half];
       const float keep = upper ? v[i + half] : v[i];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-      v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
     }
   }
 }
@@ -189,11 +228,10 @@ template <int HK, int HV>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
     const FwdParams P) {
-  constexpr int KB = HK / 64;   // K boxes (slots) per tile
-  constexpr int VB = HV / 64;   // V boxes per tile, consumed in pairs
-  constexpr int OC = HV / 128;  // O^T chunks of 128 dims
+  constexpr int KS = HK / 128;  // K slots per tile (128 dims each)
+  constexpr int VS = HV / 128;  // V slots per tile = O^T chunks of 128 dims
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kIdescQK = mma_idesc(128, kTcRows, 0, 0);
+  constexpr uint32_t kIdescQK = mma_idesc(64, kTcRows, 0, 0);
   constexpr uint32_t kIdescPV = mma_idesc(128, kTcRows, 1, 1);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
@@ -201,7 +239,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint8_t* q_s = smem + lay.q_off;
   uint8_t* p_s = smem + lay.p_off;
-  uint8_t* ring = smem + lay.ring_off;
+  uint8_t* kring = smem + lay.ring_off;
+  uint8_t* vring = kring + kTcKSlots * kTcSlotBytes;
   float* red = reinterpret_cast<float*>(smem + lay.red_off);
   float* m_used = reinterpret_cast<float*>(smem + lay.rows_off);  // [64] reference max (base 2)
   float* alpha_s = m_used + kTcRows;                              // [64] rescale factors
@@ -209,11 +248,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   int* prow = reinterpret_cast<int*>(slope2 + kTcRows);           // [64]
   float* l_tot = slope2 + 2 * kTcRows;                            // [64]
   int* flags = reinterpret_cast<int*>(l_tot + kTcRows);           // [1] rescale this tile
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars_off);
-  uint64_t* empty = full + kTcSlots;
-  uint64_t* s_full = empty + kTcSlots;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* o_done = s_full + 2;
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + lay.bars_off);
+  uint64_t* kempty = kfull + kTcKSlots;
+  uint64_t* vfull = kempty + kTcKSlots;
+  uint64_t* vempty = vfull + kTcVSlots;
+  uint64_t* s_full = vempty + kTcVSlots;  // [2] S^T buffer ready
+  uint64_t* s_free = s_full + 2;          // [2] S^T buffer read by every softmax warp
+  uint64_t* p_full = s_full + 4;          // [2] P^T buffer written
+  uint64_t* pv_done = s_full + 6;         // [2] PV that read P^T buffer b complete
+  uint64_t* qk_done = s_full + 8;         // every QK MMA complete
+  uint64_t* o_done = s_full + 9;          // every PV MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.tmem_slot_off);
 
   Item it;
@@ -226,12 +270,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
 
   // ---- set-up: barriers, TMEM, query tile, per-row constants
   if (tid == 0) {
-    for (int s = 0; s < kTcSlots; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kTcKSlots; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 4);
+    for (int s = 0; s < kTcVSlots; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 8);
+      mbar_init(&p_full[b], 8);
+      mbar_init(&pv_done[b], 1);
+    }
+    mbar_init(qk_done, 1);
     mbar_init(o_done, 1);
     fence_barrier_init();
     flags[1] = 0;
@@ -243,15 +296,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   // Q tile: row r of the tile, chunk c (8 dims) -> box c/8, swizzled position.
-  for (int idx = tid; idx < kTcRows * (HK / 8); idx += kTcThreads) {
-    const int r = idx / (HK / 8), c = idx % (HK / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < it.nrows) {
-      const int rr = it.r0 + r;
-      v = *reinterpret_cast<const uint4*>(
-          P.query + (int64_t(it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G) * HK + c * 8);
+  // All of this thread's loads are issued before any store.
+  {
+    constexpr int kChunks = kTcRows * (HK / 8);
+    constexpr int kPer = (kChunks + kTcThreads - 1) / kTcThreads;
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = tid + k * kTcThreads;
+      const int r = idx / (HK / 8), c = idx % (HK / 8);
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (idx < kChunks && r < it.nrows) {
+        const int rr = it.r0 + r;
+        v[k] = *reinterpret_cast<const uint4*>(
+            P.query + (int64_t(it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G) * HK + c * 8);
+      }
     }
-    *reinterpret_cast<uint4*>(q_s + (c >> 3) * (kTcRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = tid + k * kTcThreads;
+      const int r = idx / (HK / 8), c = idx % (HK / 8);
+      if (idx < kChunks)
+        *reinterpret_cast<uint4*>(q_s + (c >> 3) * (kTcRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v[k];
+    }
   }
   for (int r = tid; r < kTcRows; r += kTcThreads) {
     const bool ok = r < it.nrows;
@@ -266,12 +333,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem;        // S^T: columns [0, 64)
-  const uint32_t tmem_o = tmem + 64;   // O^T chunk c: columns [64 + 64 c, 128 + 64 c)
+  const uint32_t tmem_s = tmem;        // S^T buffer b: columns [64 b, 64 b + 64)
+  const uint32_t tmem_o = tmem + 128;  // O^T chunk c: columns [128 + 64 c, 192 + 64 c)
 
-  if (warp == 0) {
-    // ================= TMA producer (lane 0) =================
+  if (warp == 0 || warp == 10) {
+    // ================= TMA producers (lane 0): K (warp 0), V (warp 10) =========
     if (lane == 0) {
+      const bool is_k = warp == 0;
+      const int nslots = is_k ? kTcKSlots : kTcVSlots;
+      uint8_t* ring = is_k ? kring : vring;
+      uint64_t* full = is_k ? kfull : vfull;
+      uint64_t* empty = is_k ? kempty : vempty;
+      const CUtensorMap* map = is_k ? &tmk : &tmv;
+      const int per_tile = is_k ? KS : VS;
+      const int zbase = it.kvh * ((is_k ? HK : HV) / 64);
       const uint64_t pol = policy_evict_first();
       const int32_t* bt_row = P.block_tables + int64_t(it.b) * P.max_blocks_per_seq;
       const int box_rows = bs < kTcTok ? bs : kTcTok;
@@ -279,228 +354,290 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       int issued = 0;
       bool ok = true;
       for (int n = 0; n < ntiles && ok; ++n) {
-        const int t0 = it.tok0 + n * kTcTok;  // first token of the tile
-        for (int part = 0; part < KB + VB; ++part) {
-          const int slot = issued % kTcSlots;
-          if (!mbar_wait(&empty[slot], ((issued / kTcSlots) & 1) ^ 1)) {
+        // physical rows of the tile's pieces (-1: past the range or a bad entry)
+        const int t0 = it.tok0 + n * kTcTok;
+        int ph[4], rws[4];
+        for (int pc = 0; pc < pieces; ++pc) {
+          const int tok = t0 + pc * box_rows;
+          ph[pc] = tok < it.tok1 ? bt_row[tok / bs] : -1;
+        }
+        uint32_t bytes = 0;
+        for (int pc = 0; pc < pieces; ++pc) {
+          const int tok = t0 + pc * box_rows;
+          rws[pc] = -1;
+          if (tok >= it.tok1) continue;
+          if (ph[pc] < 0 || ph[pc] >= P.num_blocks) {
+            if (is_k) set_status(P.status, PA_STATUS_BIT_BLOCK_INDEX);
+            continue;
+          }
+          rws[pc] = ph[pc] * bs + tok % bs;
+          bytes += uint32_t(box_rows) * 256;
+        }
+        for (int sl = 0; sl < per_tile; ++sl) {
+          const int slot = issued % nslots;
+          if (!mbar_wait(&empty[slot], ((issued / nslots) & 1) ^ 1)) {
             ok = false;
             break;
           }
-          const bool is_k = part < KB;
-          const int box = is_k ? part : part - KB;
           uint8_t* dst = ring + slot * kTcSlotBytes;
-          // pieces of box_rows tokens from consecutive blocks; those past the
-          // range are not loaded (their rows are masked or zeroed later)
-          uint32_t bytes = 0;
-          int phys[8];
-          for (int pc = 0; pc < pieces; ++pc) {
-            const int tok = t0 + pc * box_rows;
-            phys[pc] = -1;
-            if (tok < it.tok1) {
-              const int ph = bt_row[tok / bs];
-              if (ph < 0 || ph >= P.num_blocks) {
-                set_status(P.status, PA_STATUS_BIT_BLOCK_INDEX);
-              } else {
-                phys[pc] = ph;
-                bytes += uint32_t(box_rows) * 128;
-              }
-            }
-          }
           if (bytes) {
             mbar_arrive_expect_tx(&full[slot], bytes);
           } else {
             mbar_arrive(&full[slot]);
           }
+          const int z = zbase + 2 * sl;  // first 64-dim half of this slot
           for (int pc = 0; pc < pieces; ++pc) {
-            if (phys[pc] < 0) continue;
-            const int tok = t0 + pc * box_rows;
-            const int row = phys[pc] * bs + tok % bs;
-            tma_load_2d(dst + pc * box_rows * 128, is_k ? &tmk : &tmv, &full[slot],
-                        it.kvh * (is_k ? HK : HV) + box * 64, row, pol);
+            if (rws[pc] < 0) continue;
+            if (box_rows == kTcTok) {
+              // one box carries both halves: [2][64 tokens][128 B] = the slot
+              tma_load_3d(dst, map, &full[slot], 0, rws[pc], z, pol);
+            } else {
+              // block_size < 64: the map's box is one half; place each half
+              tma_load_3d(dst + pc * box_rows * 128, map, &full[slot], 0, rws[pc], z, pol);
+              tma_load_3d(dst + kTcHalfBytes + pc * box_rows * 128, map, &full[slot], 0, rws[pc],
+                          z + 1, pol);
+            }
           }
           ++issued;
         }
       }
       if (!ok) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
       // let every issued copy land before the CTA can exit (bounded waits)
-      for (int i = issued - kTcSlots > 0 ? issued - kTcSlots : 0; i < issued; ++i)
-        mbar_wait(&full[i % kTcSlots], (i / kTcSlots) & 1);
+      for (int i = issued - nslots > 0 ? issued - nslots : 0; i < issued; ++i)
+        mbar_wait(&full[i % nslots], (i / nslots) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ================= MMA issuer =================
-    int consumed = 0;
+    // ================= QK issuer =================
+    // S^T(m) into buffer m & 1 once the softmax has read S^T(m - 2).
     bool ok = true;
-    const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s), ring_addr = smem_u32(ring);
-    for (int n = 0; n < ntiles && ok; ++n) {
-      // S^T = K . Q^T over the KB boxes of 64 dims (4 k-steps of 16 each)
-      for (int kb = 0; kb < KB; ++kb, ++consumed) {
-        const int slot = consumed % kTcSlots;
-        if (!warp_wait(&full[slot], (consumed / kTcSlots) & 1, lane)) { ok = false; break; }
+    const uint32_t q_addr = smem_u32(q_s), ring_addr = smem_u32(kring);
+    int consumed = 0;
+    for (int m = 0; m < ntiles && ok; ++m) {
+      if (m >= 2 && !warp_wait(&s_free[m & 1], ((m >> 1) - 1) & 1, lane)) { ok = false; break; }
+      tc_fence_after();
+      for (int ks = 0; ks < KS; ++ks, ++consumed) {
+        const int slot = consumed % kTcKSlots;
+        if (!warp_wait(&kfull[slot], (consumed / kTcKSlots) & 1, lane)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = smem_desc(ring_addr + slot * kTcSlotBytes + k * 32, 16, 1024);
-            const uint64_t b = smem_desc(q_addr + kb * (kTcRows * 128) + k * 32, 16, 1024);
-            tc_mma(tmem_s, a, b, kIdescQK, (kb | k) != 0);
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t a = smem_desc(ring_addr + slot * kTcSlotBytes + h * kTcHalfBytes + k * 32, 16, 1024);
+              const uint64_t b = smem_desc(q_addr + (2 * ks + h) * (kTcRows * 128) + k * 32, 16, 1024);
+              tc_mma(tmem_s + (m & 1) * 64, a, b, kIdescQK, (ks | h | k) != 0);
+            }
           }
-          tc_commit(&empty[slot]);
+          tc_commit(&kempty[slot]);
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(s_full);
+      if (lane == 0) tc_commit(&s_full[m & 1]);
       __syncwarp();
-      // O^T += V^T . P^T once the softmax has written P^T
-      if (!warp_wait(p_full, n & 1, lane)) { ok = false; break; }
+    }
+    if (!ok && lane == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
+    if (lane == 0) tc_commit(qk_done);
+    __syncwarp();
+  } else if (warp == 11) {
+    // ================= PV issuer =================
+    bool ok = true;
+    const uint32_t p_addr = smem_u32(p_s), ring_addr = smem_u32(vring);
+    int consumed = 0;
+    for (int n = 0; n < ntiles && ok; ++n) {
+      if (!warp_wait(&p_full[n & 1], (n >> 1) & 1, lane)) { ok = false; break; }
       tc_fence_after();
       const int nvalid = min(kTcTok, it.tok1 - (it.tok0 + n * kTcTok));
-      for (int oc = 0; oc < OC; ++oc, consumed += 2) {
-        const int s0 = consumed % kTcSlots, s1 = (consumed + 1) % kTcSlots;
-        if (!warp_wait(&full[s0], (consumed / kTcSlots) & 1, lane) ||
-            !warp_wait(&full[s1], ((consumed + 1) / kTcSlots) & 1, lane)) { ok = false; break; }
+      for (int oc = 0; oc < VS; ++oc, ++consumed) {
+        const int slot = consumed % kTcVSlots;
+        if (!warp_wait(&vfull[slot], (consumed / kTcVSlots) & 1, lane)) { ok = false; break; }
         if (nvalid < kTcTok) {
           // V rows of tokens past the range may hold anything (NaN included):
-          // zero them so that p = 0 really contributes nothing.
-          for (int idx = lane; idx < (kTcTok - nvalid) * 8 * 2; idx += 32) {
-            const int sl = idx / ((kTcTok - nvalid) * 8) ? s1 : s0;
-            const int rem = idx % ((kTcTok - nvalid) * 8);
-            *reinterpret_cast<uint4*>(ring + sl * kTcSlotBytes + (nvalid + rem / 8) * 128 +
-                                      (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+          // zero them (both 64-dim halves) so that p = 0 contributes nothing.
+          const int per = (kTcTok - nvalid) * 8;
+          for (int idx = lane; idx < 2 * per; idx += 32) {
+            const int h = idx / per, rem = idx % per;
+            *reinterpret_cast<uint4*>(vring + slot * kTcSlotBytes + h * kTcHalfBytes +
+                                      (nvalid + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async();
           __syncwarp();
         }
         tc_fence_after();
         if (lane == 0) {
-          // the pair of boxes is adjacent only when s1 == s0 + 1 (slots are
-          // consumed in pairs from an even index, and the ring size is even)
 #pragma unroll
           for (int k = 0; k < kTcTok / 16; ++k) {
-            const uint64_t a = smem_desc(ring_addr + s0 * kTcSlotBytes + k * 2048, kTcSlotBytes, 1024);
-            const uint64_t b = smem_desc(p_addr + k * 2048, kTcSlotBytes, 1024);
+            const uint64_t a = smem_desc(ring_addr + slot * kTcSlotBytes + k * 2048, kTcHalfBytes, 1024);
+            const uint64_t b = smem_desc(p_addr + (n & 1) * (kTcTok * 128) + k * 2048, kTcHalfBytes, 1024);
             tc_mma(tmem_o + oc * 64, a, b, kIdescPV, (n | k) != 0);
           }
-          tc_commit(&empty[s0]);
-          tc_commit(&empty[s1]);
+          tc_commit(&vempty[slot]);
         }
         __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&pv_done[n & 1]);
+      __syncwarp();
     }
     if (!ok && lane == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
-    if (lane == 0) tc_commit(o_done);  // completes when every MMA above is done
+    if (lane == 0) tc_commit(o_done);  // completes when every PV MMA above is done
     __syncwarp();
   } else {
-    // ================= softmax warps 2-5 =================
+    // ================= softmax warps 2-9 =================
     const int quarter = warp & 3;             // TMEM lane quarter of this warp
-    const int t = quarter * 32 + lane;        // token within the tile (= TMEM lane)
+    const int rh = (warp - 2) >> 2;           // which 32 of the 64 rows
+    const bool active = lane < 16;            // M=64: lanes 0-15 of a quarter hold tokens
+    const int tt = quarter * 16 + lane;       // token within the tile (active lanes)
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    float l_part[2] = {0.f, 0.f};             // row sums of rows 2*lane, 2*lane+1 (this warp)
+    const int rbase = rh * 32;
+    // This token's probabilities summed over the tiles, for rows rbase + r,
+    // relative to the row's reference max; reduced across tokens at the end.
+    float l_t[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) l_t[r] = 0.f;
+    const float4* m_used4 = reinterpret_cast<const float4*>(m_used + rbase);
     bool ok = true;
     for (int n = 0; n < ntiles; ++n) {
-      const bool got = mbar_wait(s_full, n & 1);
-      if (softmax_bar_or(!got)) { ok = false; break; }  // all four warps agree
+      const bool got = mbar_wait(&s_full[n & 1], (n >> 1) & 1);
+      if (softmax_bar_or(!got)) { ok = false; break; }  // all softmax warps agree
       tc_fence_after();
-      float s[64];
-      tmem_ld32(tmem_s + lane_base, s);
-      tmem_ld32(tmem_s + lane_base + 32, s + 32);
+      float s[32];
+      tmem_ld32(tmem_s + (n & 1) * 64 + lane_base + rbase, s);
       tmem_wait_ld();
-      const int j = it.tok0 + n * kTcTok + t;
-      const bool tok_ok = j < it.tok1;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[n & 1]);  // this S^T buffer may be rewritten
+      const int j = it.tok0 + n * kTcTok + tt;
+      const bool tok_ok = active && j < it.tok1;
+      // scores in base 2, plus bias; tokens past the range drop out
+      if (P.mask_type == PA_MASK_ALIBI) {
 #pragma unroll
-      for (int r = 0; r < 64; ++r) {
-        float v = s[r] * P.scale_log2;
-        if (P.mask_type == PA_MASK_ALIBI) {
-          v += slope2[r] * float(j - prow[r]);
-        } else if (P.mask_type == PA_MASK_NORM_COMPRESS) {
-          if (tok_ok && j > prefix) {
-            const int mr = min(max(prow[r] - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
-            const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
-            v += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
-          }
-        }
-        s[r] = tok_ok ? v : -INFINITY;
-      }
-      // tile max per row: reduce-scatter in the warp, then across the 4 warps
-      float w[64];
+        for (int r = 0; r < 32; ++r)
+          s[r] = s[r] * P.scale_log2 + slope2[rbase + r] * float(j - prow[rbase + r]);
+      } else {
 #pragma unroll
-      for (int r = 0; r < 64; ++r) w[r] = s[r];
-      reduce_scatter64<true>(w, lane);
-      red[quarter * 64 + 2 * lane] = w[0];
-      red[quarter * 64 + 2 * lane + 1] = w[1];
-      softmax_bar();
-      if (warp == 2) {
-        // reference max update for rows 2*lane, 2*lane+1 (lazy rescale)
-        bool grow = false;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int r = 2 * lane + e;
-          const float mt = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
-          const float mu = m_used[r];
-          float a = 1.f;
-          if (mt > mu + kTcRescaleThreshold || mu == -INFINITY) {
-            const float nm = fmaxf(mt, mu);
-            a = ex2(mu - nm);  // 0 on the first tile
-            m_used[r] = nm;
-            grow = grow || (mu != -INFINITY);
-          }
-          alpha_s[r] = a;
-        }
-        grow = __any_sync(0xffffffffu, grow);
-        if (lane == 0) flags[1] = grow ? 1 : 0;
-      }
-      softmax_bar();
-      const bool rescale = flags[1] != 0;
-      if (rescale) {
-        // O^T rows of this thread's TMEM lane (= output dims) times alpha per column;
-        // PV of the previous tile is complete: S^T of this tile was committed after it.
-        l_part[0] *= alpha_s[2 * lane];
-        l_part[1] *= alpha_s[2 * lane + 1];
+        for (int r = 0; r < 32; ++r) s[r] *= P.scale_log2;
+        if (P.mask_type == PA_MASK_NORM_COMPRESS && tok_ok && j > prefix) {
+          const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
 #pragma unroll 1
-        for (int oc = 0; oc < OC; ++oc) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float o[32];
-            const uint32_t ta = tmem_o + oc * 64 + h * 32 + lane_base;
-            tmem_ld32(ta, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha_s[h * 32 + i];
-            tmem_st32(ta, o);
+          for (int r = 0; r < 32; ++r) {
+            const int mr = min(max(prow[rbase + r] - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
+            s[r] += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
           }
+        }
+      }
+      if (!tok_ok) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) s[r] = -INFINITY;
+      }
+      // Is any score above its row's reference max by more than the threshold?
+      // (Always on the first tile, where the references are -inf.)
+      float ex = -INFINITY;
+#pragma unroll
+      for (int r4 = 0; r4 < 8; ++r4) {
+        const float4 m = m_used4[r4];
+        ex = fmaxf(ex, fmaxf(fmaxf(s[4 * r4] - m.x, s[4 * r4 + 1] - m.y),
+                             fmaxf(s[4 * r4 + 2] - m.z, s[4 * r4 + 3] - m.w)));
+      }
+      bool grew = false;
+      if (softmax_bar_or(ex > kTcRescaleThreshold)) {
+        // exact tile max per row: warp max, then across the 4 lane quarters
+        float keep = 0.f;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+          const float wm = warp_max(s[r]);
+          if (r == lane) keep = wm;
+        }
+        red[quarter * 64 + rbase + lane] = keep;
+        softmax_bar();
+        if (warp == 2) {
+          bool grow = false;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int r = lane + 32 * e;
+            const float mt = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
+            const float mu = m_used[r];
+            const float nm = fmaxf(mt, mu);
+            alpha_s[r] = ex2(mu - nm);  // 0 on the first tile
+            m_used[r] = nm;
+            grow = grow || (mu != -INFINITY && nm != mu);
+          }
+          grow = __any_sync(0xffffffffu, grow);
+          if (lane == 0) flags[1] = grow ? 1 : 0;
+        }
+        softmax_bar();
+        grew = flags[1] != 0;
+        if (grew) {
+#pragma unroll
+          for (int r = 0; r < 32; ++r) l_t[r] *= alpha_s[rbase + r];
+        }
+      }
+      // probabilities and per-token sums
+#pragma unroll
+      for (int r4 = 0; r4 < 8; ++r4) {
+        const float4 m = m_used4[r4];
+        s[4 * r4] = ex2(s[4 * r4] - m.x);
+        s[4 * r4 + 1] = ex2(s[4 * r4 + 1] - m.y);
+        s[4 * r4 + 2] = ex2(s[4 * r4 + 2] - m.z);
+        s[4 * r4 + 3] = ex2(s[4 * r4 + 3] - m.w);
+      }
+#pragma unroll
+      for (int r = 0; r < 32; ++r) l_t[r] += s[r];
+      // P^T buffer n & 1 was last read by PV(n - 2); a rescale of O^T also
+      // needs PV(n - 1). Each wait is on the barrier of that PV's P^T buffer.
+      {
+        bool pv = true;
+        if (grew && n >= 1) pv = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1);
+        if (n >= 2) pv = pv && mbar_wait(&pv_done[n & 1], ((n - 2) >> 1) & 1);
+        if (softmax_bar_or(!pv)) { ok = false; break; }
+        tc_fence_after();
+      }
+      // P^T into shared memory: token row tt, rows rbase.. = 16-byte chunks
+      // 4 rh .. 4 rh + 3 of the 128-byte row
+      if (active) {
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          uint4 pk;
+          pk.x = pack_half2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
+          pk.y = pack_half2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
+          pk.z = pack_half2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
+          pk.w = pack_half2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
+          const int chunk = 4 * rh + c8;
+          *reinterpret_cast<uint4*>(p_s + (n & 1) * (kTcTok * 128) + tt * 128 + ((chunk ^ (tt & 7)) << 4)) = pk;
+        }
+      }
+      if (grew) {
+        // References grew: rescale this thread's O^T lane (an output dim) for
+        // its 32 rows, before this tile's PV (PV of the previous tile is done).
+#pragma unroll 1
+        for (int oc = 0; oc < VS; ++oc) {
+          float o[32];
+          const uint32_t ta = tmem_o + oc * 64 + rbase + lane_base;
+          tmem_ld32(ta, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha_s[rbase + i];
+          tmem_st32(ta, o);
         }
         tmem_wait_st();
       }
-      // probabilities, row sums, P^T into shared memory (token row t, 64 rows of fp16)
-#pragma unroll
-      for (int r = 0; r < 64; ++r) s[r] = ex2(s[r] - m_used[r]);
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        uint4 pk;
-        pk.x = pack_half2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
-        pk.y = pack_half2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
-        pk.z = pack_half2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
-        pk.w = pack_half2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(p_s + t * 128 + ((c8 ^ (t & 7)) << 4)) = pk;
-      }
-      reduce_scatter64<false>(s, lane);
-      l_part[0] += s[0];
-      l_part[1] += s[1];
       fence_proxy_async();  // P^T is read by the tensor cores
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[n & 1]);
     }
-    if (!ok && t == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
-    // ---- epilogue: row sums across the 4 warps, then O^T / l
-    red[quarter * 64 + 2 * lane] = l_part[0];
-    red[quarter * 64 + 2 * lane + 1] = l_part[1];
+    const int t = quarter * 32 + lane;  // TMEM lane of this thread = output dim in a chunk
+    if (!ok && t == 0 && rh == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
+    // ---- epilogue: row sums across all tokens, then O^T / l
+    reduce_scatter32_add(l_t, lane);  // lane l: rows rbase + l, this warp's tokens
+    red[quarter * 64 + rbase + lane] = l_t[0];
     softmax_bar();
     if (warp == 2) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int r = 2 * lane + e;
+        const int r = lane + 32 * e;
         l_tot[r] = (red[r] + red[64 + r]) + (red[128 + r] + red[192 + r]);
       }
     }
@@ -511,29 +648,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       tc_fence_after();
       const bool partial = it.slot >= 0;
       const bool fits = !partial || int64_t(it.slot) + it.nrows <= P.part_rows_cap;
-      if (!fits && t == 0) set_status(P.status, PA_STATUS_BIT_WORKSPACE);
+      if (!fits && t == 0 && rh == 0) set_status(P.status, PA_STATUS_BIT_WORKSPACE);
 #pragma unroll 1
-      for (int oc = 0; oc < OC; ++oc) {
+      for (int oc = 0; oc < VS; ++oc) {
         const int d = oc * 128 + t;  // output dim of this thread
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float o[32];
-          tmem_ld32(tmem_o + oc * 64 + h * 32 + lane_base, o);
-          tmem_wait_ld();
-          if (!fits) continue;
+        float o[32];
+        tmem_ld32(tmem_o + oc * 64 + rbase + lane_base, o);
+        tmem_wait_ld();
+        if (!fits) continue;
 #pragma unroll 4
-          for (int i = 0; i < 32; ++i) {
-            const int r = h * 32 + i;
-            if (r >= it.nrows) break;
-            const float val = o[i] / l_tot[r];
-            if (!partial) {
-              const int rr = it.r0 + r;
-              P.out[(int64_t(it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G) * HV + d] =
-                  __float2half_rn(val);
-            } else {
-              P.part_o[(int64_t(it.slot) + r) * HV + d] = val;
-              if (d == 0) P.part_lse[it.slot + r] = (m_used[r] + log2f(l_tot[r])) * kLn2;
-            }
+        for (int i = 0; i < 32; ++i) {
+          const int r = rbase + i;
+          if (r >= it.nrows) break;
+          const float val = o[i] / l_tot[r];
+          if (!partial) {
+            const int rr = it.r0 + r;
+            P.out[(int64_t(it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G) * HV + d] =
+                __float2half_rn(val);
+          } else {
+            P.part_o[(int64_t(it.slot) + r) * HV + d] = val;
+            if (d == 0) P.part_lse[it.slot + r] = (m_used[r] + log2f(l_tot[r])) * kLn2;
           }
         }
       }
@@ -543,7 +677,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    if (lane == 0) mbar_wait(o_done, 0);
+    if (lane == 0) {
+      mbar_wait(qk_done, 0);
+      mbar_wait(o_done, 0);
+    }
     __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
