@@ -62,12 +62,21 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sources_sha():
+# Device sources of each attention kernel: an ncu figure stays valid while
+# these files are unchanged.
+KERNEL_SOURCES = {
+    "mma_decode_kernel": ["pa_decode_mma.cuh", "pa_decode_mma.cu"],
+    "fma_decode_kernel": ["pa_decode_fma.cuh"],
+    "tc_decode_kernel": ["pa_decode_tc.cuh", "pa_decode_tc.cu"],
+}
+COMMON_SOURCES = ["pa_device.cuh", "pa_warp_pipe.cuh"]
+
+
+def kernel_sources_sha(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_206_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in COMMON_SOURCES + KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     h.update(open(os.path.join(ROOT, "include", "pa.h"), "rb").read())
     return h.hexdigest()[:16]
 
@@ -81,7 +90,7 @@ def ncu_traffic(kernel: str, workload: str):
     text = open(p).read()
     m_sha = re.search(r"^source_sha:\s*(\S+)", text, re.M)
     m_b = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-    if not (m_sha and m_b) or m_sha.group(1) != kernel_sources_sha():
+    if not (m_sha and m_b) or m_sha.group(1) != kernel_sources_sha(kernel):
         return None
     return float(m_b.group(1))
 
@@ -285,6 +294,7 @@ def main():
     kv_bytes = w.kv_bytes()
     qo_bytes = w.qo_bytes()
     n_comb = db.plan.combine.shape[0]
+    n_items = db.plan.work.shape[0]
 
     def step():
         db.forward(stream)
@@ -313,35 +323,21 @@ def main():
     # the dominant kernel alone: the same launch without the combine pass
     dec_times = time_device(decode_only, max(50, args.steps // 4), 5, flush, stream)
 
-    # end to end through the C ABI with host buffers
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    h_query = pin(w.query)
-    h_bt = pin(w.block_tables)
-    h_ctx = pin(w.context_lens)
-    h_out = torch.empty(tuple(db.out.shape), dtype=torch.float16).pin_memory()
-    ql = None if np.all(w.q_seqlens == 1) else w.q_seqlens
-    n_items = db.plan.work.shape[0]
-    h_work = torch.empty((n_items, 8), dtype=torch.int32).pin_memory()
-    h_comb = torch.empty((max(n_comb, 1), 4), dtype=torch.int32).pin_memory()
+    # end to end through the C ABI with host buffers: the step's inputs sit in
+    # one pinned host arena (query, block tables, lengths; the planner writes
+    # the work and combine lists into it), one copy moves it to the device, the
+    # output comes back into pinned memory, and the host waits for it
+    hs = pa.HostStep(db.cfg, db.key_cache, db.value_cache, w.total_q, mask=db.mask,
+                     alibi_slopes=db.alibi_slopes)
+    hs.query.copy_(torch.from_numpy(np.ascontiguousarray(w.query)))
+    hs.block_tables.copy_(torch.from_numpy(np.ascontiguousarray(w.block_tables)))
+    hs.context_lens.copy_(torch.from_numpy(np.ascontiguousarray(w.context_lens)))
+    if hs.q_seqlens is not None:
+        hs.q_seqlens.copy_(torch.from_numpy(np.ascontiguousarray(w.q_seqlens)))
 
     def e2e_step():
-        plan = pa.pa_plan(db.cfg, h_ctx.numpy(), ql)
-        h_work.numpy()[:] = plan.work
-        if n_comb:
-            h_comb.numpy()[:n_comb] = plan.combine
-        db.query.copy_(h_query, non_blocking=True)
-        db.block_tables.copy_(h_bt, non_blocking=True)
-        db.context_lens.copy_(h_ctx, non_blocking=True)
-        db.work.copy_(h_work, non_blocking=True)
-        if n_comb:
-            db.combine.copy_(h_comb[:n_comb], non_blocking=True)
-        db.forward(stream)
-        h_out.copy_(db.out, non_blocking=True)
-        stream.synchronize()
+        hs.run(stream)
 
-    h2d = (h_query.numel() * 2 + h_bt.numel() * 4 + h_ctx.numel() * 4 + h_work.numel() * 4 +
-           (n_comb * 4 * 4))
-    d2h = h_out.numel() * 2
     for _ in range(min(5, args.e2e_steps)):
         e2e_step()
     e2e_t = []
@@ -351,6 +347,15 @@ def main():
         t0 = time.perf_counter()
         e2e_step()
         e2e_t.append(time.perf_counter() - t0)
+    h2d = hs.last_h2d_bytes
+    d2h = hs.out.numel() * hs.out.element_size()
+    if e2e_t:
+        st, bits = hs.status(stream)
+        if st != pa.PA_OK:
+            raise RuntimeError(f"e2e kernel status {pa.status_string(st)} ({bits})")
+        db.forward(stream)
+        if not torch.equal(hs.out, db.out.cpu()):
+            raise RuntimeError("end-to-end output differs from the device-resident run")
 
     ms = statistics.mean(times)
     dec_ms = statistics.mean(dec_times)

@@ -33,6 +33,8 @@ PA_MASK_NORM_COMPRESS = 5
 PA_WORK_INTS = 8
 PA_COMBINE_INTS = 4
 PA_STATUS_BYTES = 256
+PA_FMA_MAX_ROWS = 8
+PA_TC_TILE_ROWS = 64
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_plan", "pa_forward", "pa_forward_noalloc", "pa_status_clear", "pa_status_read",
@@ -256,6 +258,124 @@ class DeviceBatch:
         pa_forward(self.cfg, self.query, self.key_cache, self.value_cache, self.block_tables,
                    self.context_lens, self.q_seqlens, self.mask, self.alibi_slopes, self.work,
                    self.combine, self.workspace, self.out, stream)
+        return self.out
+
+    def status(self, stream=None):
+        return pa_status_read(self.workspace, stream)
+
+
+def _align(n: int, a: int = 256) -> int:
+    return (n + a - 1) // a * a
+
+
+def list_capacity(cfg: pa_config) -> tuple[int, int]:
+    """(work items, combine entries) that hold pa_plan's lists for any context
+    and query lengths the configuration admits.
+
+    A (sequence, kv head) has at most QT = ceil(G * max_seqlen_q / TR) query
+    tiles, so there are at most B * Hk * QT combine entries. With an explicit
+    chunk c each tile has at most ceil(max_blocks_per_seq / c) splits; with the
+    automatic rule c >= W / (8 * num_sms), so the items, a sum over tiles of
+    ceil(NB / c) <= NB / c + 1, number at most 8 * num_sms + B * Hk * QT.
+    """
+    rows = (cfg.num_heads // cfg.kv_heads) * max(1, cfg.max_seqlen_q)
+    tr = rows if rows <= PA_FMA_MAX_ROWS else PA_TC_TILE_ROWS
+    tiles = cfg.batch * cfg.kv_heads * (-(-rows // tr))
+    if cfg.chunk_blocks > 0:
+        items = tiles * (-(-cfg.max_blocks_per_seq // cfg.chunk_blocks))
+    else:
+        items = 8 * cfg.num_sms + tiles
+    return items, tiles
+
+
+class HostStep:
+    """One attention step whose per-step inputs live in pinned host memory.
+
+    The caller writes the step's query, block tables, context lengths (and
+    query lengths) into the pinned views ``query``, ``block_tables``,
+    ``context_lens`` and ``q_seqlens``; :meth:`run` then plans the step
+    (pa_plan, writing the work and combine lists straight into the same pinned
+    arena), moves the used part of the arena to the device with one
+    host-to-device copy, enqueues pa_forward on device pointers into it, copies
+    the output back into the pinned ``out`` tensor and waits for the stream.
+    The KV cache, mask and ALiBi slopes stay resident on the device.
+    """
+
+    def __init__(self, cfg: pa_config, key_cache, value_cache, total_q: int, mask=None,
+                 alibi_slopes=None, device=None):
+        import torch
+        self.cfg = cfg
+        dev = key_cache.device if device is None else torch.device(device)
+        self.key_cache, self.value_cache = key_cache, value_cache
+        self.mask, self.alibi_slopes = mask, alibi_slopes
+        B, H, hk, hv = cfg.batch, cfg.num_heads, cfg.head_size_k, cfg.head_size_v
+        has_ql = cfg.max_seqlen_q > 1
+        self.total_q = int(total_q)
+        self.work_cap, ccap = list_capacity(cfg)
+        self.combine_cap = max(ccap, 1)
+        # The combine list sits before the work list so that the copied
+        # prefix ends with the items actually planned.
+        sizes = [("query", self.total_q * H * hk * 2),
+                 ("block_tables", B * cfg.max_blocks_per_seq * 4),
+                 ("context_lens", B * 4), ("q_seqlens", B * 4 if has_ql else 0),
+                 ("combine", self.combine_cap * PA_COMBINE_INTS * 4),
+                 ("work", self.work_cap * PA_WORK_INTS * 4)]
+        self.offsets, off = {}, 0
+        for name, n in sizes:
+            self.offsets[name] = off
+            off = _align(off + n)
+        self.arena_bytes = off
+        self.h_arena = torch.zeros(off, dtype=torch.uint8).pin_memory()
+        self.d_arena = torch.zeros(off, dtype=torch.uint8, device=dev)
+
+        def hview(name, dtype, shape):
+            o = self.offsets[name]
+            n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            return self.h_arena[o:o + n].view(dtype).view(shape)
+
+        self.query = hview("query", torch.float16, (self.total_q, H, hk))
+        self.block_tables = hview("block_tables", torch.int32, (B, cfg.max_blocks_per_seq))
+        self.context_lens = hview("context_lens", torch.int32, (B,))
+        self.q_seqlens = hview("q_seqlens", torch.int32, (B,)) if has_ql else None
+        self.out = torch.empty((self.total_q, H, hv), dtype=torch.float16).pin_memory()
+        self.d_out = torch.empty((self.total_q, H, hv), dtype=torch.float16, device=dev)
+        self._d = {k: self.d_arena.data_ptr() + v for k, v in self.offsets.items()}
+        self._h = {k: self.h_arena.data_ptr() + v for k, v in self.offsets.items()}
+        self.workspace = None
+        self.last_h2d_bytes = 0
+        self.n_items = self.n_combine = 0
+
+    def run(self, stream=None):
+        """Plan, copy in, attend, copy out; returns the pinned ``out`` tensor."""
+        import torch
+        lib = load_library()
+        cfg, h, d, P = self.cfg, self._h, self._d, ctypes.c_void_p
+        has_ql = self.q_seqlens is not None
+        n_items, n_comb, ws = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_size_t()
+        _check(lib.pa_plan(ctypes.byref(cfg), P(h["context_lens"]),
+                           P(h["q_seqlens"]) if has_ql else None, P(h["work"]), self.work_cap,
+                           ctypes.byref(n_items), P(h["combine"]), self.combine_cap,
+                           ctypes.byref(n_comb), ctypes.byref(ws)), "pa_plan")
+        self.n_items, self.n_combine = n_items.value, n_comb.value
+        need = max(int(ws.value), PA_STATUS_BYTES)
+        if self.workspace is None or self.workspace.numel() < need:
+            self.workspace = torch.zeros(need, dtype=torch.uint8, device=self.d_arena.device)
+        used = self.offsets["work"] + self.n_items * PA_WORK_INTS * 4
+        self.last_h2d_bytes = used
+        s = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(s):
+            self.d_arena[:used].copy_(self.h_arena[:used], non_blocking=True)
+        st = lib.pa_forward(ctypes.byref(cfg), P(d["query"]), _tptr(self.key_cache),
+                            _tptr(self.value_cache), P(d["block_tables"]), P(d["context_lens"]),
+                            P(d["q_seqlens"]) if has_ql else None, _tptr(self.mask),
+                            _tptr(self.alibi_slopes), P(d["work"]), self.n_items,
+                            P(d["combine"]) if self.n_combine else None, self.n_combine,
+                            _tptr(self.workspace), self.workspace.numel(), _tptr(self.d_out),
+                            ctypes.c_void_p(s.cuda_stream))
+        _check(st, "pa_forward")
+        with torch.cuda.stream(s):
+            self.out.copy_(self.d_out, non_blocking=True)
+        s.synchronize()
         return self.out
 
     def status(self, stream=None):

@@ -53,20 +53,85 @@ BoxGeom box_geom(bool wide) {
   return {16, 1u, CU_TENSOR_MAP_SWIZZLE_32B};
 }
 
+// Encoded tensor maps of recent calls, keyed by everything the encoding reads,
+// so that a steady stream of pa_forward calls on the same caches does not
+// re-encode them.
+struct MapKey {
+  const void* base;
+  uint64_t dims[3];
+  uint32_t box[3];
+  int rank, swizzle;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && rank == o.rank && swizzle == o.swizzle && dims[0] == o.dims[0] &&
+           dims[1] == o.dims[1] && dims[2] == o.dims[2] && box[0] == o.box[0] &&
+           box[1] == o.box[1] && box[2] == o.box[2];
+  }
+};
+
+class MapCache {
+ public:
+  bool get(const MapKey& k, CUtensorMap* out) {
+    std::lock_guard<std::mutex> lock(mu_);
+    for (int i = 0; i < kEntries; ++i)
+      if (used_[i] && keys_[i] == k) {
+        *out = maps_[i];
+        return true;
+      }
+    return false;
+  }
+  void put(const MapKey& k, const CUtensorMap& m) {
+    std::lock_guard<std::mutex> lock(mu_);
+    keys_[next_] = k;
+    maps_[next_] = m;
+    used_[next_] = true;
+    next_ = (next_ + 1) % kEntries;
+  }
+
+ private:
+  static constexpr int kEntries = 16;
+  std::mutex mu_;
+  MapKey keys_[kEntries];
+  CUtensorMap maps_[kEntries];
+  bool used_[kEntries] = {};
+  int next_ = 0;
+};
+
+MapCache& map_cache() {
+  static MapCache c;
+  return c;
+}
+
+// The map for key k (fp16 elements; the row stride follows from the dims).
+bool cached_map(CUtensorMap* m, const MapKey& k, const cuuint64_t* strides) {
+  if (map_cache().get(k, m)) return true;
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {k.dims[0], k.dims[1], k.dims[2]};
+  cuuint32_t box[3] = {k.box[0], k.box[1], k.box[2]};
+  cuuint32_t es[3] = {1, 1, 1};
+  if (enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, cuuint32_t(k.rank), const_cast<void*>(k.base), dims,
+          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CUtensorMapSwizzle(k.swizzle),
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  map_cache().put(k, *m);
+  return true;
+}
+
 // The cache [num_blocks, bs, Hk, hs] viewed as a 2-D tensor of
 // num_blocks * bs token rows by Hk * hs elements; a box is box_rows tokens of
 // one box-width slice of one kv head.
 bool cache_map(CUtensorMap* m, const void* base, const pa_config& c, int hs, int box_rows,
                const BoxGeom& g) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cuuint64_t(c.kv_heads) * hs, cuuint64_t(c.num_blocks) * c.block_size};
-  cuuint64_t strides[1] = {cuuint64_t(c.kv_heads) * hs * 2};
-  cuuint32_t box[2] = {cuuint32_t(g.width), cuuint32_t(box_rows)};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, g.swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  MapKey k{};
+  k.base = base;
+  k.rank = 2;
+  k.swizzle = int(g.swizzle);
+  k.dims[0] = uint64_t(c.kv_heads) * hs;
+  k.dims[1] = uint64_t(c.num_blocks) * c.block_size;
+  k.box[0] = uint32_t(g.width);
+  k.box[1] = uint32_t(box_rows);
+  const cuuint64_t strides[2] = {cuuint64_t(c.kv_heads) * hs * 2, 0};
+  return cached_map(m, k, strides);
 }
 
 // The same cache as a 3-D tensor for the tcgen05 kernel: dims (64 elements of
@@ -75,16 +140,18 @@ bool cache_map(CUtensorMap* m, const void* base, const pa_config& c, int hs, int
 // dims, each landing as its own [box_rows][128 B] swizzled tile.
 bool cache_map_3d(CUtensorMap* m, const void* base, const pa_config& c, int hs, int box_rows,
                   int halves) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {64, cuuint64_t(c.num_blocks) * c.block_size,
-                        cuuint64_t(c.kv_heads) * (hs / 64)};
-  cuuint64_t strides[2] = {cuuint64_t(c.kv_heads) * hs * 2, 128};
-  cuuint32_t box[3] = {64, cuuint32_t(box_rows), cuuint32_t(halves)};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  MapKey k{};
+  k.base = base;
+  k.rank = 3;
+  k.swizzle = int(CU_TENSOR_MAP_SWIZZLE_128B);
+  k.dims[0] = 64;
+  k.dims[1] = uint64_t(c.num_blocks) * c.block_size;
+  k.dims[2] = uint64_t(c.kv_heads) * (hs / 64);
+  k.box[0] = 64;
+  k.box[1] = uint32_t(box_rows);
+  k.box[2] = uint32_t(halves);
+  const cuuint64_t strides[2] = {cuuint64_t(c.kv_heads) * hs * 2, 128};
+  return cached_map(m, k, strides);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -16,6 +16,7 @@
 #pragma once
 
 #include "pa_warp_pipe.cuh"
+#include "pa_launch.h"
 
 namespace pa {
 
@@ -296,8 +297,7 @@ cudaError_t launch_fma(const CUtensorMap& tmk, const CUtensorMap& tmv, const Fwd
   const int vc = (P.hv / 8 + 31) / 32;
   const bool wide = (P.hk % 64 == 0) && (P.hv % 64 == 0);
   auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(lay.bytes));
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), int(lay.bytes));
     if (e != cudaSuccess) return e;
     kern<<<unsigned(n_items), nw * 32, lay.bytes, stream>>>(tmk, tmv, P);
     return cudaGetLastError();

@@ -1,5 +1,6 @@
 // Instantiations and launcher of the mma.sync decode kernel.
 #include "pa_decode_mma.cuh"
+#include "pa_launch.h"
 
 namespace pa {
 
@@ -8,8 +9,7 @@ cudaError_t launch_mma(const CUtensorMap& tmk, const CUtensorMap& tmv, const Fwd
   const int nw = mma_warps(P.hk, P.hv);
   const PipeLayout lay = pipe_layout(nw, kMmaBufs, P.hk, P.hv, 0, 8);
   auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(lay.bytes));
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), int(lay.bytes));
     if (e != cudaSuccess) return e;
     kern<<<unsigned(n_items), nw * 32, lay.bytes, stream>>>(tmk, tmv, P);
     return cudaGetLastError();

@@ -1,5 +1,6 @@
 // Instantiations and launcher of the tcgen05 decode kernel (64-row tiles).
 #include "pa_decode_tc.cuh"
+#include "pa_launch.h"
 
 namespace pa {
 
@@ -7,8 +8,7 @@ cudaError_t launch_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdP
                       int64_t n_items, cudaStream_t stream) {
   const TcLayout lay = tc_layout(P.hk);
   auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(lay.bytes));
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), int(lay.bytes));
     if (e != cudaSuccess) return e;
     kern<<<unsigned(n_items), kTcThreads, lay.bytes, stream>>>(tmk, tmv, P);
     return cudaGetLastError();

@@ -171,3 +171,33 @@ def test_constraint_errors(lib, kw, ctx, ql, expect):
     kw = dict(kw)
     kw.setdefault("batch", len(ctx))
     assert status_of(cfg(**kw), ctx, ql) == expect
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_list_capacity_bounds_every_plan(lib, seed):
+    """pa.list_capacity, the list sizes HostStep reserves, bounds the lists of
+    any lengths the configuration admits: all full, all one block, a mix, and
+    lengths just past a chunk boundary (the worst case for ceil(NB / c))."""
+    rng = np.random.default_rng(100 + seed)
+    H = int(rng.choice([4, 8, 32, 64]))
+    Hk = int(rng.choice([d for d in (1, 2, 4, 8) if H % d == 0]))
+    bs = int(rng.choice([16, 32, 128]))
+    maxq = int(rng.choice([1, 2, 4, 9]))
+    B = int(rng.integers(1, 200))
+    maxnb = int(rng.integers(1, 300))
+    chunk = int(rng.choice([0, 0, 1, 5]))
+    c = cfg(batch=B, num_heads=H, kv_heads=Hk, block_size=bs, max_seqlen_q=maxq,
+            chunk_blocks=chunk, max_blocks_per_seq=maxnb, num_sms=int(rng.choice([1, 152])))
+    wcap, ccap = pa.list_capacity(c)
+    ql = None if maxq == 1 else np.full(B, maxq, np.int32)
+    floor = maxq if ql is not None else 1
+    trials = [np.full(B, maxnb * bs), np.full(B, 1), rng.integers(1, maxnb * bs + 1, size=B)]
+    n = pa.pa_plan(c, np.maximum(trials[0], floor).astype(np.int32), ql)
+    # lengths with NB = k*c + 1 for the chunk the full plan chose
+    cc = max(1, int(n.work[0, 5] - n.work[0, 4]))
+    nb = np.minimum(maxnb, (rng.integers(0, maxnb // cc + 1, size=B) * cc + 1))
+    trials.append(nb * bs - bs + 1)
+    for ctx in trials:
+        p = pa.pa_plan(c, np.maximum(ctx, floor).astype(np.int32), ql)
+        assert p.work.shape[0] <= wcap
+        assert p.combine.shape[0] <= ccap
