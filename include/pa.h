@@ -28,6 +28,12 @@
  *                          triangle 0; the shift keeps both indices inside the
  *                          mask for any L_b, so sequences longer than 2048 need
  *                          nothing extra from the caller).
+ *   PA_MASK_NORM           mask[b][i][j], the model's own additive mask
+ *                          ("How to select a mask", PA_ENCODER restrictions
+ *                          page), given per sequence as fp16
+ *                          [batch][max_seqlen_q][max_blocks_per_seq * bs];
+ *                          the kernels read the entries with i < q_b and
+ *                          j < L_b only.
  * The mask value is added to the scaled score, not substituted by -inf, and is
  * not scaled. The kernels read the mask only where j > L_b - q_b: every other
  * element they would read lies on or below the diagonal, which the pages fix
@@ -68,8 +74,8 @@ typedef enum pa_status {
 
 /* Mask types. 5 is MASK_TYPE_NORM_COMPRESS as numbered by the pages; the
  * pages name UNDEFINED, NORM and ALIBI without numbers, so 0/1/2 are ours.
- * 1 (full mask of the real max_seq_len) and 4 (a spec-decoding mask whose
- * contents the pages do not describe) return PA_ERR_UNSUPPORTED. */
+ * 4 (a spec-decoding mask whose contents the pages do not describe) returns
+ * PA_ERR_UNSUPPORTED. */
 typedef enum pa_mask_type {
   PA_MASK_NONE = 0,
   PA_MASK_NORM = 1,
@@ -195,11 +201,20 @@ pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens, const int32
  *
  * query         device fp16 [sum q_b, H, hk]
  * key_cache     device fp16 [num_blocks, bs, Hk, hk]; 16-byte aligned
- * value_cache   device fp16 [num_blocks, bs, Hk, hv]; 16-byte aligned
+ * value_cache   device fp16 [num_blocks, bs, Hk, hv]; 16-byte aligned. Or
+ *               exactly key_cache (requires hv <= hk): the shared-KV layout,
+ *               one cache whose K row also carries V, V_b[j] being the first
+ *               hv dims of K_b[j] (the latent cache of MLA-style models, K of
+ *               576 dims and V of 512 in the head-size rule of the
+ *               "Constraints" page). The CUDA-core and mma.sync kernels then
+ *               fetch each row once; the tensor-core kernel reads the V dims
+ *               of a row a second time, normally from L2.
  * block_tables  device int32 [batch, max_blocks_per_seq]
  * context_lens  device int32 [batch]
  * q_seqlens     device int32 [batch], or NULL when every q_b = 1
- * mask          device fp16 [2048, 2048]; non-NULL exactly for NORM_COMPRESS
+ * mask          device fp16 [2048, 2048] for NORM_COMPRESS, or
+ *               [batch, max_seqlen_q, max_blocks_per_seq * bs] for NORM;
+ *               non-NULL exactly for those two types
  * alibi_slopes  device fp32 [H]; non-NULL exactly for ALIBI
  * work/combine  device copies of pa_plan's lists (same cfg, same lengths)
  * workspace     device, >= pa_plan's workspace_bytes, 256-byte aligned; its
@@ -209,8 +224,9 @@ pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens, const int32
  * stream        a cudaStream_t (NULL = legacy default stream)
  *
  * Host-side errors return before anything is enqueued. Block-table entries
- * outside [0, num_blocks) are never dereferenced: the kernel reads zeros in
- * their place and sets PA_STATUS_BIT_BLOCK_INDEX, which pa_status_read reports.
+ * outside [0, num_blocks) are never dereferenced: the kernel skips their
+ * copies, leaving the affected outputs undefined, and sets
+ * PA_STATUS_BIT_BLOCK_INDEX, which pa_status_read reports.
  */
 pa_status pa_forward(const pa_config* cfg, const void* query, const void* key_cache,
                      const void* value_cache, const int32_t* block_tables,

@@ -42,7 +42,8 @@ def _load():
         P = ctypes.c_void_p
         i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.oracle_attention.restype = i32
-        lib.oracle_attention.argtypes = [i32] * 9 + [dbl] + [P] * 8 + [P, i32, P, i32]
+        lib.oracle_attention.argtypes = ([i32] * 9 + [dbl] + [P] * 7 + [i64, i64]
+                                         + [P] + [P, i32, P, i32])
         lib.oracle_plan.restype = i32
         lib.oracle_plan.argtypes = [i32] * 9 + [P, P, P, i64, P, P, i64, P, P]
         lib.oracle_half_to_double.restype = dbl
@@ -73,6 +74,10 @@ def attention(w, subset=None, threads: int = 1, out: np.ndarray | None = None):
     cl = np.ascontiguousarray(w.context_lens, dtype=np.int32)
     ql = np.ascontiguousarray(w.q_seqlens, dtype=np.int32)
     mask = None if w.mask is None else np.ascontiguousarray(w.mask)
+    mask_q = mask_kv = 0
+    if w.mask_type == 1:  # MASK_TYPE_NORM: [batch, max q, max_blocks_per_seq * block_size]
+        assert mask.shape == (w.batch, w.max_seqlen_q, w.max_blocks_per_seq * w.block_size)
+        mask_q, mask_kv = mask.shape[1], mask.shape[2]
     slopes = None if w.alibi_slopes is None else np.ascontiguousarray(w.alibi_slopes, dtype=np.float32)
     if out is None:
         out = np.zeros((w.total_q, w.num_heads, w.head_size_v), dtype=np.float64)
@@ -82,7 +87,7 @@ def attention(w, subset=None, threads: int = 1, out: np.ndarray | None = None):
         w.num_blocks, w.max_blocks_per_seq, w.mask_type, float(w.scale),
         _ptr(q.view(np.uint16)), _ptr(kc.view(np.uint16)), _ptr(vc.view(np.uint16)),
         _ptr(bt), _ptr(cl), _ptr(ql), None if mask is None else _ptr(mask.view(np.uint16)),
-        _ptr(slopes), _ptr(sub), 0 if sub is None else len(sub), _ptr(out), int(threads))
+        mask_q, mask_kv, _ptr(slopes), _ptr(sub), 0 if sub is None else len(sub), _ptr(out), int(threads))
     if used < 0:
         raise ValueError("oracle: unsupported head size")
     return out, used

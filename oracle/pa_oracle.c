@@ -20,7 +20,11 @@
  *   - the compressed 2048 x 2048 mask is applied with the shift
  *     sigma = max(0, L - 2048): bias = mask[p - sigma][j - sigma] for
  *     j >= sigma, else 0 (it "adapts automatically" to longer sequences);
- *   - ALiBi bias = slope_h * (j - p).
+ *   - ALiBi bias = slope_h * (j - p);
+ *   - MASK_TYPE_NORM (the model's own mask, "How to select a mask") is an
+ *     explicit additive tensor per sequence: bias = mask[b][i][j] for query
+ *     token i and key j, the tensor being [batch][mask_q][mask_kv] with
+ *     mask_q = max_seqlen_q and mask_kv = max_blocks_per_seq * block_size.
  * The oracle reads the whole mask row it needs, lower triangle included; for a
  * mask as the pages define it that part is zero. For mask tensors that break
  * that definition the oracle and the kernels may differ: parity unpinned there.
@@ -53,13 +57,14 @@ double oracle_half_to_double(uint16_t h) {
   return sign ? -v : v;
 }
 
-enum { MASK_NONE = 0, MASK_ALIBI = 2, MASK_NORM_COMPRESS = 5 };
+enum { MASK_NONE = 0, MASK_NORM = 1, MASK_ALIBI = 2, MASK_NORM_COMPRESS = 5 };
 #define MASK_DIM 2048
 
 typedef struct {
   int batch, num_heads, kv_heads, hk, hv, block_size, num_blocks, max_blocks_per_seq;
   int mask_type;
   double scale;
+  int64_t mask_q, mask_kv; /* MASK_NORM tensor dims after the batch */
 } oracle_shape;
 
 /* One (sequence, kv head) unit: gather, then every head of the group and
@@ -105,6 +110,8 @@ static void unit(const oracle_shape* S, int b, int kvh, const uint16_t* query,
         } else if (S->mask_type == MASK_NORM_COMPRESS) {
           if (j >= sigma)
             bias = oracle_half_to_double(mask[(int64_t)(p - sigma) * MASK_DIM + (j - sigma)]);
+        } else if (S->mask_type == MASK_NORM) {
+          bias = oracle_half_to_double(mask[((int64_t)b * S->mask_q + i) * S->mask_kv + j]);
         }
         s[j] = S->scale * dot + bias;
       }
@@ -141,10 +148,11 @@ int oracle_attention(int batch, int num_heads, int kv_heads, int hk, int hv, int
                      const uint16_t* query, const uint16_t* key_cache,
                      const uint16_t* value_cache, const int32_t* block_tables,
                      const int32_t* context_lens, const int32_t* q_seqlens,
-                     const uint16_t* mask, const float* alibi_slopes, const int32_t* subset,
-                     int n_subset, double* out, int threads) {
+                     const uint16_t* mask, int64_t mask_q, int64_t mask_kv,
+                     const float* alibi_slopes, const int32_t* subset, int n_subset,
+                     double* out, int threads) {
   oracle_shape S = {batch, num_heads, kv_heads, hk, hv, block_size, num_blocks,
-                    max_blocks_per_seq, mask_type, scale};
+                    max_blocks_per_seq, mask_type, scale, mask_q, mask_kv};
   if (hk > 1024) return -1;
   int64_t* q_start = (int64_t*)malloc(sizeof(int64_t) * (size_t)(batch + 1));
   q_start[0] = 0;

@@ -241,7 +241,8 @@ class DeviceBatch:
 
         self.query = up(w.query)
         self.key_cache = up(w.key_cache)
-        self.value_cache = up(w.value_cache)
+        # shared-KV cache: the value pointer is the key cache itself
+        self.value_cache = self.key_cache if w.shared_kv else up(w.value_cache)
         self.block_tables = up(w.block_tables)
         self.context_lens = up(w.context_lens)
         self.q_seqlens = up(ql_host)

@@ -173,11 +173,15 @@ extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const v
   if (!query || !key_cache || !value_cache || !block_tables || !context_lens || !out ||
       !workspace)
     return PA_ERR_INVALID_ARG;
-  if ((c.mask_type == PA_MASK_NORM_COMPRESS) != (mask != nullptr)) return PA_ERR_INVALID_ARG;
+  const bool has_mask = c.mask_type == PA_MASK_NORM_COMPRESS || c.mask_type == PA_MASK_NORM;
+  if (has_mask != (mask != nullptr)) return PA_ERR_INVALID_ARG;
   if ((c.mask_type == PA_MASK_ALIBI) != (alibi_slopes != nullptr)) return PA_ERR_INVALID_ARG;
   if (n_items < 0 || n_combine < 0 || n_items > INT32_MAX || n_combine > INT32_MAX)
     return PA_ERR_INVALID_ARG;
   if ((n_items > 0 && !work) || (n_combine > 0 && !combine)) return PA_ERR_INVALID_ARG;
+  // value_cache == key_cache: the shared-KV layout, V = first hv dims of each K row
+  const bool kv_shared = value_cache == key_cache;
+  if (kv_shared && c.head_size_v > c.head_size_k) return PA_ERR_INVALID_ARG;
   if (!aligned(query, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
       !aligned(out, 16) || !aligned(workspace, 256))
     return PA_ERR_INVALID_ARG;
@@ -212,6 +216,9 @@ extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const v
   P.max_blocks_per_seq = c.max_blocks_per_seq;
   P.num_blocks = c.num_blocks;
   P.mask_type = c.mask_type;
+  P.kv_shared = kv_shared ? 1 : 0;
+  P.mask_q = int(max_q(c));
+  P.mask_kv = int64_t(c.max_blocks_per_seq) * c.block_size;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / std::sqrt(float(hk));
   P.scale_log2 = scale * kLog2e;
 
@@ -220,7 +227,10 @@ extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const v
     const bool wide = (hk % 64 == 0) && (hv % 64 == 0);
     const BoxGeom kg = box_geom(wide), vg = box_geom(wide);
     CUtensorMap tmk, tmv;
-    if (!cache_map(&tmk, key_cache, c, hk, 16, kg) || !cache_map(&tmv, value_cache, c, hv, 16, vg))
+    // (with a shared-KV cache the warp kernels read V from the K boxes; the
+    // V map is then built over the K rows and left unused)
+    if (!cache_map(&tmk, key_cache, c, hk, 16, kg) ||
+        !cache_map(&tmv, value_cache, c, kv_shared ? hk : hv, 16, vg))
       return PA_ERR_CUDA;
     if (TR >= 2 && mma_supported(hk, hv)) {
       err = launch_mma(tmk, tmv, P, n_items, stream);
@@ -238,7 +248,7 @@ extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const v
     const int halves = rows == 64 ? 2 : 1;
     CUtensorMap tmk, tmv;
     if (!cache_map_3d(&tmk, key_cache, c, hk, rows, halves) ||
-        !cache_map_3d(&tmv, value_cache, c, hv, rows, halves))
+        !cache_map_3d(&tmv, value_cache, c, kv_shared ? hk : hv, rows, halves))
       return PA_ERR_CUDA;
     err = launch_tc(tmk, tmv, P, n_items, stream);
   }

@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(128) fma_decode_kernel(const __grid_constant__
           const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
           x += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
         }
+      } else if (P.mask_type == PA_MASK_NORM) {
+        if (tok_ok) x += norm_mask_log2(P, it.b, prow[rr] - prefix, j);
       }
       x = tok_ok ? x : -INFINITY;
       float mt = x;

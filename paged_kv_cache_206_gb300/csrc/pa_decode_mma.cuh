@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(128) mma_decode_kernel(const __grid_constant__
           const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
           v += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
         }
+      } else if (P.mask_type == PA_MASK_NORM) {
+        if (tok < nvalid) v += norm_mask_log2(P, it.b, prow[col] - prefix, j);
       }
       x[e] = tok < nvalid ? v : -INFINITY;
     }

@@ -17,6 +17,7 @@ cudaError_t launch_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdP
     case 128128: return go(tc_decode_kernel<128, 128>);
     case 256256: return go(tc_decode_kernel<256, 256>);
     case 512512: return go(tc_decode_kernel<512, 512>);
+    case 576512: return go(tc_decode_kernel<576, 512>);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -87,9 +87,9 @@ __host__ __device__ inline TcLayout tc_layout(int hk) {
 }
 
 // Head-size pairs the tcgen05 kernel is instantiated for (K and V move in
-// 128-dim halves of a 16 KB box).
+// 16 KB slots of 64 tokens x 128 dims; a 576-dim K row takes four and a half).
 inline bool tc_supported(int hk, int hv) {
-  return hk == hv && (hk == 128 || hk == 256 || hk == 512);
+  return (hk == hv && (hk == 128 || hk == 256 || hk == 512)) || (hk == 576 && hv == 512);
 }
 
 // ---- tcgen05 / TMEM primitives --------------------------------------------
@@ -228,7 +228,9 @@ template <int HK, int HV>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
     const FwdParams P) {
-  constexpr int KS = HK / 128;  // K slots per tile (128 dims each)
+  constexpr int KH = HK / 64;         // 64-dim halves of a K row
+  constexpr int KS = (KH + 1) / 2;    // K slots per tile (128 dims each; the
+                                      // last holds one half when KH is odd)
   constexpr int VS = HV / 128;  // V slots per tile = O^T chunks of 128 dims
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kIdescQK = mma_idesc(64, kTcRows, 0, 0);
@@ -346,7 +348,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       uint64_t* empty = is_k ? kempty : vempty;
       const CUtensorMap* map = is_k ? &tmk : &tmv;
       const int per_tile = is_k ? KS : VS;
-      const int zbase = it.kvh * ((is_k ? HK : HV) / 64);
+      // 64-dim blocks per kv head in the map's rows: a shared-KV V map spans the K rows
+      const int zbase = it.kvh * ((is_k || P.kv_shared ? HK : HV) / 64);
       const uint64_t pol = policy_evict_first();
       const int32_t* bt_row = P.block_tables + int64_t(it.b) * P.max_blocks_per_seq;
       const int box_rows = bs < kTcTok ? bs : kTcTok;
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
           const int tok = t0 + pc * box_rows;
           ph[pc] = tok < it.tok1 ? bt_row[tok / bs] : -1;
         }
-        uint32_t bytes = 0;
+        int npieces = 0;
         for (int pc = 0; pc < pieces; ++pc) {
           const int tok = t0 + pc * box_rows;
           rws[pc] = -1;
@@ -371,9 +374,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
             continue;
           }
           rws[pc] = ph[pc] * bs + tok % bs;
-          bytes += uint32_t(box_rows) * 256;
+          ++npieces;
         }
         for (int sl = 0; sl < per_tile; ++sl) {
+          // the last K slot of an odd number of halves carries one half; a
+          // 64-token box still moves two (the second is the next 64 dims of
+          // the row, or the fill value past the tensor) and is left unread
+          const bool one_half = is_k && (KH & 1) && sl == KS - 1 && box_rows != kTcTok;
+          const uint32_t bytes = uint32_t(npieces) * box_rows * (one_half ? 128 : 256);
           const int slot = issued % nslots;
           if (!mbar_wait(&empty[slot], ((issued / nslots) & 1) ^ 1)) {
             ok = false;
@@ -394,8 +402,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
             } else {
               // block_size < 64: the map's box is one half; place each half
               tma_load_3d(dst + pc * box_rows * 128, map, &full[slot], 0, rws[pc], z, pol);
-              tma_load_3d(dst + kTcHalfBytes + pc * box_rows * 128, map, &full[slot], 0, rws[pc],
-                          z + 1, pol);
+              if (!one_half)
+                tma_load_3d(dst + kTcHalfBytes + pc * box_rows * 128, map, &full[slot], 0,
+                            rws[pc], z + 1, pol);
             }
           }
           ++issued;
@@ -423,6 +432,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         if (lane == 0) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
+            if (2 * ks + h >= KH) break;  // an odd KH leaves the last slot one half
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint64_t a = smem_desc(ring_addr + slot * kTcSlotBytes + h * kTcHalfBytes + k * 32, 16, 1024);
@@ -521,11 +531,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         for (int r = 0; r < 32; ++r) s[r] *= P.scale_log2;
         if (P.mask_type == PA_MASK_NORM_COMPRESS && tok_ok && j > prefix) {
           const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
-#pragma unroll 1
+#pragma unroll
           for (int r = 0; r < 32; ++r) {
             const int mr = min(max(prow[rbase + r] - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
             s[r] += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
           }
+        } else if (P.mask_type == PA_MASK_NORM && tok_ok) {
+#pragma unroll
+          for (int r = 0; r < 32; ++r) s[r] += norm_mask_log2(P, it.b, prow[rbase + r] - prefix, j);
         }
       }
       if (!tok_ok) {
@@ -656,7 +669,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         tmem_ld32(tmem_o + oc * 64 + rbase + lane_base, o);
         tmem_wait_ld();
         if (!fits) continue;
-#pragma unroll 4
+#pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int r = rbase + i;
           if (r >= it.nrows) break;

@@ -166,7 +166,15 @@ struct FwdParams {
   int64_t part_rows_cap;
   int num_heads, kv_heads, group, hk, hv, block_size, max_blocks_per_seq, num_blocks;
   int mask_type;
+  int kv_shared;     // V of a token = the first hv dims of its K row (value_cache == key_cache)
+  int mask_q;        // PA_MASK_NORM: mask is [batch][mask_q][mask_kv]
+  int64_t mask_kv;
   float scale_log2;  // scale * log2(e)
 };
+
+// Bias (base 2) of a PA_MASK_NORM mask for query token i of sequence b and key j.
+__device__ __forceinline__ float norm_mask_log2(const FwdParams& P, int b, int i, int j) {
+  return __half2float(P.mask[(int64_t(b) * P.mask_q + i) * P.mask_kv + j]) * kLog2e;
+}
 
 }  // namespace pa

@@ -36,11 +36,11 @@ pa_status validate_config(const pa_config* cfg) {
   switch (c.mask_type) {
     case PA_MASK_NONE:
     case PA_MASK_ALIBI:
+    case PA_MASK_NORM:
       break;
     case PA_MASK_NORM_COMPRESS:
       if (max_q(c) > PA_COMPRESS_MASK_SIZE) return PA_ERR_INVALID_ARG;
       break;
-    case PA_MASK_NORM:
     case PA_MASK_SPEC:
       return PA_ERR_UNSUPPORTED;
     default:

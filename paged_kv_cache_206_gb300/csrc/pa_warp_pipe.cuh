@@ -85,6 +85,7 @@ struct WarpPipe {
   const int32_t* bt_row;
   int bt_base, bt_reg;
   int kb0, kb1, warp, nw, lane, bs, hk, hv, kvh, num_blocks, nkbox, nvbox;
+  bool shared;  // V is read from the K boxes (shared-KV cache): no V copies
   uint32_t* status;
   uint64_t pol;
   const CUtensorMap* tmk;
@@ -102,7 +103,8 @@ struct WarpPipe {
     v_off = lay.v_in_buf;
     hk = P.hk;
     hv = P.hv;
-    tile_bytes = uint32_t(kSubTokens) * (hk + hv) * 2;
+    shared = P.kv_shared != 0;
+    tile_bytes = uint32_t(kSubTokens) * (hk + (shared ? 0 : hv)) * 2;
     nkbox = hk / KBW;
     nvbox = hv / VBW;
     bs = P.block_size;
@@ -128,7 +130,9 @@ struct WarpPipe {
   // Sub-tile index (within the item) of this warp's n-th sub-tile.
   __device__ __forceinline__ int sub(int n) const { return warp + n * nw; }
   __device__ __forceinline__ uint8_t* kbuf(int n) const { return bufs + (n % NBUF) * stride; }
-  __device__ __forceinline__ uint8_t* vbuf(int n) const { return kbuf(n) + v_off; }
+  // With a shared-KV cache the V sub-tile is the first hv / VBW boxes of the
+  // K sub-tile (K and V boxes have the same width, so the same layout).
+  __device__ __forceinline__ uint8_t* vbuf(int n) const { return shared ? kbuf(n) : kbuf(n) + v_off; }
 
   // Start the copies of this warp's n-th sub-tile into buffer n % NBUF.
   __device__ __forceinline__ void issue(int n) {
@@ -155,8 +159,9 @@ struct WarpPipe {
       mbar_arrive_expect_tx(bar, tile_bytes);
       for (int j = 0; j < nkbox; ++j)
         tma_load_2d(dst + j * kBoxBytes, tmk, bar, kvh * hk + j * KBW, row, pol);
-      for (int j = 0; j < nvbox; ++j)
-        tma_load_2d(dst + v_off + j * vBoxBytes, tmv, bar, kvh * hv + j * VBW, row, pol);
+      if (!shared)
+        for (int j = 0; j < nvbox; ++j)
+          tma_load_2d(dst + v_off + j * vBoxBytes, tmv, bar, kvh * hv + j * VBW, row, pol);
     }
   }
 

@@ -28,6 +28,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 MASK_NONE = 0
+MASK_NORM = 1
 MASK_ALIBI = 2
 MASK_NORM_COMPRESS = 5
 
@@ -55,7 +56,7 @@ class Workload:
     query: np.ndarray  # fp16 [sum q, H, hk]
     key_cache: np.ndarray  # fp16 [nb, bs, Hk, hk]
     value_cache: np.ndarray  # fp16 [nb, bs, Hk, hv]
-    mask: np.ndarray | None = None  # fp16 [2048, 2048]
+    mask: np.ndarray | None = None  # fp16 [2048, 2048], or [B, max q, maxNB * bs] (NORM)
     alibi_slopes: np.ndarray | None = None  # fp32 [H]
     chunk_blocks: int = 0
     meta: dict = field(default_factory=dict)
@@ -72,10 +73,15 @@ class Workload:
     def total_q(self) -> int:
         return int(self.q_seqlens.sum())
 
+    @property
+    def shared_kv(self) -> bool:
+        return bool(self.meta.get("shared_kv", False))
+
     def kv_bytes(self) -> int:
-        """Bytes of K and V that attention must read: sum_b L_b * Hk * (hk + hv) * 2."""
-        return int(self.context_lens.astype(np.int64).sum()) * self.kv_heads * (
-            self.head_size_k + self.head_size_v) * 2
+        """Bytes of K and V that attention must read: sum_b L_b * Hk * (hk + hv) * 2,
+        or sum_b L_b * Hk * hk * 2 when V is part of the K rows (shared cache)."""
+        per = self.head_size_k + (0 if self.shared_kv else self.head_size_v)
+        return int(self.context_lens.astype(np.int64).sum()) * self.kv_heads * per * 2
 
     def qo_bytes(self) -> int:
         """Bytes of query read plus output written (fp16)."""
@@ -127,6 +133,26 @@ def alibi_slopes(num_heads: int) -> np.ndarray:
     return np.exp2(-8.0 * (h + 1.0) / num_heads).astype(np.float32)
 
 
+def norm_mask(context_lens, q_seqlens, max_kv: int, seed: int, bias_std: float = 0.5,
+              fill: float = -10000.0) -> np.ndarray:
+    """A MASK_TYPE_NORM tensor fp16 [B, max q, max_kv]: for query token i of
+    sequence b (position p = L - q + i) and key j < L, a seeded N(0, bias_std^2)
+    bias where j <= p and ``fill`` above the diagonal; entries outside the
+    sequence (i >= q or j >= L) are NaN, so reading one shows up in the result."""
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    ql = np.asarray(q_seqlens, dtype=np.int64)
+    B, maxq = ctx.shape[0], int(ql.max())
+    rng = np.random.default_rng(seed)
+    m = np.full((B, maxq, max_kv), np.nan, dtype=np.float16)
+    for b in range(B):
+        L, q = int(ctx[b]), int(ql[b])
+        pos = (L - q + np.arange(q))[:, None]
+        j = np.arange(L)[None, :]
+        bias = rng.normal(0.0, bias_std, size=(q, L))
+        m[b, :q, :L] = np.where(j <= pos, bias, fill).astype(np.float16)
+    return m
+
+
 def make_workload(
     name: str,
     *,
@@ -147,6 +173,7 @@ def make_workload(
     mask_fill: float = -10000.0,
     poison_unused: bool = True,
     scale: float | None = None,
+    shared_kv: bool = False,
 ) -> Workload:
     """Build one seeded workload.
 
@@ -157,8 +184,14 @@ def make_workload(
     of every entry. Cache slots no sequence uses (the tail of each last block
     and the spare blocks) are set to NaN when ``poison_unused``, so reading one
     shows up in the result.
+
+    ``shared_kv``: one cache holds both, V of a token being the first
+    ``head_size_v`` dims of its K row (the MLA-style latent cache); the device
+    run passes the K cache as the value cache, and ``value_cache`` here is the
+    explicit copy of those dims that the oracle reads.
     """
     head_size_v = head_size_k if head_size_v is None else head_size_v
+    assert not shared_kv or head_size_v <= head_size_k
     ctx = np.asarray(context_lens, dtype=np.int32).reshape(-1)
     B = ctx.shape[0]
     ql = (np.ones(B, dtype=np.int32) if q_seqlens is None
@@ -183,10 +216,12 @@ def make_workload(
     total_q = int(ql.sum())
     query = np.empty((total_q, num_heads, head_size_k), dtype=np.float16)
     kc = np.empty((num_blocks, block_size, kv_heads, head_size_k), dtype=np.float16)
-    vc = np.empty((num_blocks, block_size, kv_heads, head_size_v), dtype=np.float16)
+    vc = None if shared_kv else np.empty((num_blocks, block_size, kv_heads, head_size_v),
+                                          dtype=np.float16)
     _fill_normal(query, seed * 7 + 1, std)
     _fill_normal(kc, seed * 7 + 2, std)
-    _fill_normal(vc, seed * 7 + 3, std)
+    if vc is not None:
+        _fill_normal(vc, seed * 7 + 3, std)
 
     if poison_unused:
         used = np.zeros(num_blocks, dtype=bool)
@@ -197,11 +232,20 @@ def make_workload(
             tail = int(ctx[b]) - (n - 1) * block_size  # valid slots in the last block
             if tail < block_size:
                 kc[blocks[n - 1], tail:] = np.float16(np.nan)
-                vc[blocks[n - 1], tail:] = np.float16(np.nan)
+                if vc is not None:
+                    vc[blocks[n - 1], tail:] = np.float16(np.nan)
         kc[~used] = np.float16(np.nan)
-        vc[~used] = np.float16(np.nan)
+        if vc is not None:
+            vc[~used] = np.float16(np.nan)
+    if shared_kv:
+        vc = np.ascontiguousarray(kc[..., :head_size_v])
 
-    mask = compress_mask(mask_fill) if mask_type == MASK_NORM_COMPRESS else None
+    if mask_type == MASK_NORM_COMPRESS:
+        mask = compress_mask(mask_fill)
+    elif mask_type == MASK_NORM:
+        mask = norm_mask(ctx, ql, maxnb * block_size, seed * 7 + 4, fill=mask_fill)
+    else:
+        mask = None
     slopes = alibi_slopes(num_heads) if mask_type == MASK_ALIBI else None
     if scale is None:
         scale = 1.0 / math.sqrt(head_size_k)
@@ -212,7 +256,7 @@ def make_workload(
         context_lens=ctx, q_seqlens=ql, block_tables=tables, query=query,
         key_cache=kc, value_cache=vc, mask=mask, alibi_slopes=slopes,
         chunk_blocks=chunk_blocks,
-        meta={"seed": seed, "std": std},
+        meta={"seed": seed, "std": std, "shared_kv": bool(shared_kv)},
     )
 
 
@@ -259,10 +303,21 @@ def mqa_split(seed: int = 0, batch: int = 8, ctx_len: int = 32768, chunk_blocks:
                          chunk_blocks=chunk_blocks)
 
 
+def mla_decode(seed: int = 0, batch: int = 64, max_len: int = 8192) -> Workload:
+    """MLA-style decode on a shared-KV latent cache: B=64, H=16, Hk=1, K rows
+    of 576 dims whose first 512 are V, bs=64, L ~ U[1,8192], q=1, N(0, 0.5^2)."""
+    rng = np.random.default_rng(seed + 4000)
+    ctx = rng.integers(1, max_len + 1, size=batch, dtype=np.int32)
+    return make_workload("mla_decode", context_lens=ctx, num_heads=16, kv_heads=1,
+                         head_size_k=576, head_size_v=512, block_size=64, std=0.5, seed=seed,
+                         shared_kv=True)
+
+
 NAMED = {
     "tiny_decode": tiny_decode,
     "gqa_decode": gqa_decode,
     "spec_decode": spec_decode,
     "alibi_decode": alibi_decode,
     "mqa_split": mqa_split,
+    "mla_decode": mla_decode,
 }

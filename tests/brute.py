@@ -11,7 +11,7 @@ the causal mask and its fill value, GQA).
 """
 import numpy as np
 
-MASK_NONE, MASK_ALIBI, MASK_NORM_COMPRESS = 0, 2, 5
+MASK_NONE, MASK_NORM, MASK_ALIBI, MASK_NORM_COMPRESS = 0, 1, 2, 5
 
 
 def full_causal_rows(L, q, fill):
@@ -39,6 +39,8 @@ def attention(w, mask_fill=-10000.0):
             S = w.scale * (Q[:, h, :] @ K[:, kv, :].T)                 # [q, L]
             if w.mask_type == MASK_NORM_COMPRESS:
                 S = S + full_causal_rows(L, q, mask_fill)
+            elif w.mask_type == MASK_NORM:
+                S = S + w.mask[b, :q, :L].astype(np.float64)
             elif w.mask_type == MASK_ALIBI:
                 pos = (L - q + np.arange(q))[:, None]
                 S = S + float(w.alibi_slopes[h]) * (j[None, :] - pos)

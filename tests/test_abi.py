@@ -82,6 +82,8 @@ def test_forward_host_checks(lib):
     assert _fwd(lib, c, mask=fake) == pa.PA_ERR_INVALID_ARG          # mask only with NORM_COMPRESS
     assert _fwd(lib, _cfg(mask_type=5)) == pa.PA_ERR_INVALID_ARG     # NORM_COMPRESS needs a mask
     assert _fwd(lib, _cfg(mask_type=2)) == pa.PA_ERR_INVALID_ARG     # ALIBI needs slopes
+    assert _fwd(lib, _cfg(mask_type=1)) == pa.PA_ERR_INVALID_ARG     # NORM needs its mask
+    assert _fwd(lib, _cfg(mask_type=1), mask=fake, n_items=0, work=None) == pa.PA_OK
     assert _fwd(lib, c, slopes=fake) == pa.PA_ERR_INVALID_ARG
     assert _fwd(lib, _cfg(mask_type=4)) == pa.PA_ERR_UNSUPPORTED
     assert _fwd(lib, _cfg(block_size=8)) == pa.PA_ERR_INVALID_ARG
@@ -91,5 +93,11 @@ def test_forward_host_checks(lib):
     assert _fwd(lib, c, n_comb=1, comb=None) == pa.PA_ERR_INVALID_ARG
     assert _fwd(lib, c, n_items=-1) == pa.PA_ERR_INVALID_ARG
     assert _fwd(lib, c, n_items=0, work=None) == pa.PA_OK              # nothing to do
+    # value_cache == key_cache is the shared-KV layout: V = first hv dims of a
+    # K row, so hv may not exceed hk; distinct caches have no such rule
+    wide_v = _cfg(head_size_v=128)
+    assert _fwd(lib, wide_v, n_items=0, work=None) == pa.PA_ERR_INVALID_ARG
+    other = ctypes.c_void_p((1 << 21))
+    assert _fwd(lib, wide_v, value=other, n_items=0, work=None) == pa.PA_OK
     assert lib.pa_status_clear(None, None) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_status_read(None, None, None) == pa.PA_ERR_INVALID_ARG

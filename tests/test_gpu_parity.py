@@ -100,6 +100,25 @@ CASES = {
                                             block_size=16, mask_type=W.MASK_ALIBI, seed=12),
     "bs16_long": lambda: W.make_workload("bs16", context_lens=[4000, 1, 17], num_heads=4,
                                          kv_heads=4, head_size_k=128, block_size=16, seed=13),
+    # MASK_TYPE_NORM: a per-sequence [q, L] additive mask (NaN outside the
+    # sequence, so a read past q or L shows): CUDA-core, mma.sync paths
+    "norm_q1": lambda: W.make_workload("n1", context_lens=[70, 513, 1], num_heads=3, kv_heads=3,
+                                       head_size_k=128, block_size=32, mask_type=W.MASK_NORM,
+                                       seed=17),
+    "norm_spec_gqa": lambda: W.make_workload("n2", context_lens=[40, 900, 3], q_seqlens=[3, 2, 3],
+                                             num_heads=4, kv_heads=2, head_size_k=128,
+                                             block_size=64, mask_type=W.MASK_NORM, seed=18),
+    # shared-KV caches on the warp-pipelined kernels (V read from the K boxes):
+    # mma.sync with 576/512 and 4 rows, CUDA-core with 64-wide and 16-wide boxes
+    "mma_mla_shared": lambda: W.make_workload("mmas", context_lens=[900, 77, 16], num_heads=4,
+                                              kv_heads=1, head_size_k=576, head_size_v=512,
+                                              block_size=64, std=0.5, seed=14, shared_kv=True),
+    "fma_shared_hd128": lambda: W.make_workload("fs", context_lens=[333, 40], num_heads=2,
+                                                kv_heads=2, head_size_k=128, head_size_v=64,
+                                                block_size=32, seed=15, shared_kv=True),
+    "fma_shared_hk96": lambda: W.make_workload("fs96", context_lens=[129, 500], num_heads=3,
+                                               kv_heads=3, head_size_k=96, head_size_v=48,
+                                               block_size=16, seed=16, shared_kv=True),
 }
 
 
@@ -176,6 +195,24 @@ TC_CASES = {
     # block_size 256: a tile is half a block
     "tc_bs256": lambda: W.make_workload("tc256", context_lens=[600, 256, 257], num_heads=16,
                                         kv_heads=1, head_size_k=128, block_size=256, seed=35),
+    # MASK_TYPE_NORM on the tensor-core path: 16 heads x 2 tokens per kv head
+    "tc_norm": lambda: W.make_workload("tcn", context_lens=[300, 1200], q_seqlens=[2, 1],
+                                       num_heads=16, kv_heads=1, head_size_k=128, block_size=64,
+                                       mask_type=W.MASK_NORM, seed=39, chunk_blocks=6),
+    # MLA-style shared-KV cache: K rows of 576 dims, V = their first 512
+    "tc_mla_shared": lambda: W.make_workload("mla", context_lens=[700, 1500, 65], num_heads=16,
+                                             kv_heads=1, head_size_k=576, head_size_v=512,
+                                             block_size=64, std=0.5, seed=36, shared_kv=True,
+                                             chunk_blocks=8),
+    # 576/512 with separate caches and two kv heads: the half-slot of kv head
+    # 0 reads kv head 1's first dims, that of kv head 1 reads past the tensor
+    "tc_hk576_two_heads": lambda: W.make_workload("tc576", context_lens=[300, 129], num_heads=32,
+                                                  kv_heads=2, head_size_k=576, head_size_v=512,
+                                                  block_size=128, std=0.5, seed=37),
+    # 576/512 shared with 16-token blocks: the half slot moves as one box per block
+    "tc_mla_bs16": lambda: W.make_workload("mla16", context_lens=[200, 33], num_heads=64,
+                                           kv_heads=1, head_size_k=576, head_size_v=512,
+                                           block_size=16, std=0.5, seed=38, shared_kv=True),
 }
 
 
@@ -214,7 +251,8 @@ def sample_rows(w, k, seed):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["gqa_decode", "spec_decode", "alibi_decode", "mqa_split"])
+@pytest.mark.parametrize("name", ["gqa_decode", "spec_decode", "alibi_decode", "mqa_split",
+                                  "mla_decode"])
 def test_full_size_sampled(oracle_mod, name):
     w = W.NAMED[name]()
     got, db = run_gpu(w)

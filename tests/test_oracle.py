@@ -53,6 +53,10 @@ def test_half_decode_all_bit_patterns(oracle_mod):
          mask_type=W.MASK_ALIBI),
     dict(context_lens=[12, 40], num_heads=4, kv_heads=2, head_size_k=32, head_size_v=16),
     dict(context_lens=[20], num_heads=2, kv_heads=2, head_size_k=16, scale=0.37),
+    dict(context_lens=[9, 50], num_heads=4, kv_heads=2, head_size_k=16,
+         mask_type=W.MASK_NORM),
+    dict(context_lens=[6, 33, 70], q_seqlens=[3, 1, 4], num_heads=6, kv_heads=3,
+         head_size_k=16, mask_type=W.MASK_NORM, block_size=32),
 ])
 def test_oracle_matches_brute_force(oracle_mod, case):
     w = small(**case)
@@ -221,3 +225,34 @@ def test_subset_computes_only_listed_sequences(oracle_mod):
     assert np.array_equal(sub[[0, 3]], full[[0, 3]])
     assert np.all(sub[1:3] == 0)
     assert 1 <= used <= 2
+
+
+def _causal_norm(w, bias_std):
+    """Replace w's NORM mask by one with the given bias spread (0: a plain causal mask)."""
+    w.mask = W.norm_mask(w.context_lens, w.q_seqlens, w.max_blocks_per_seq * w.block_size,
+                         seed=99, bias_std=bias_std)
+    return w
+
+
+def test_norm_causal_mask_equals_compressed_mask(oracle_mod):
+    """A per-sequence NORM mask holding the plain causal mask gives what the
+    compressed 2048 x 2048 mask gives, below and past 2048 keys."""
+    for L, q in ((1, 1), (40, 4), (2048, 3), (2049, 2), (3000, 5)):
+        w = small(context_lens=[L, 17], q_seqlens=[q, 1], num_heads=2, kv_heads=1,
+                  block_size=64, mask_type=W.MASK_NORM, seed=L)
+        norm = run(oracle_mod, _causal_norm(w, 0.0))
+        w.mask_type, w.mask = W.MASK_NORM_COMPRESS, W.compress_mask()
+        np.testing.assert_array_equal(norm, run(oracle_mod, w), err_msg=f"L={L} q={q}")
+
+
+def test_norm_bias_is_read_per_sequence_and_token(oracle_mod):
+    """A bias on one (sequence, query token, key) entry changes exactly that
+    output row: a transposed or mis-strided read would move it."""
+    w = small(context_lens=[30, 45], q_seqlens=[2, 3], num_heads=2, kv_heads=2,
+              mask_type=W.MASK_NORM, seed=21)
+    w = _causal_norm(w, 0.0)
+    base = run(oracle_mod, w)
+    w.mask[1, 2, 7] = np.float16(3.0)  # sequence 1, query token 2 (global row 4), key 7
+    got = run(oracle_mod, w)
+    changed = np.abs(got - base).max(axis=(1, 2)) > 0
+    assert changed.tolist() == [False, False, False, False, True]

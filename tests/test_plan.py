@@ -157,7 +157,6 @@ def status_of(c, ctx, ql=None):
     (dict(max_seqlen_q=2), [10] * 4, [3, 1, 1, 1], pa.PA_ERR_INVALID_ARG),         # q <= max
     (dict(), [0, 1, 1, 1], None, pa.PA_ERR_INVALID_ARG),               # L >= 1
     (dict(max_blocks_per_seq=2), [33, 1, 1, 1], None, pa.PA_ERR_INVALID_ARG),  # table too narrow
-    (dict(mask_type=1), [10] * 4, None, pa.PA_ERR_UNSUPPORTED),        # full mask: not built
     (dict(mask_type=4), [10] * 4, None, pa.PA_ERR_UNSUPPORTED),        # spec mask: unspecified
     (dict(mask_type=3), [10] * 4, None, pa.PA_ERR_INVALID_ARG),
     (dict(mask_type=5, max_seqlen_q=2049, block_size=16), [3000] * 4, [2049] * 4,
