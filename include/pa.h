@@ -95,6 +95,7 @@ typedef enum pa_mask_type {
 #define PA_STATUS_BIT_BLOCK_INDEX 1u
 #define PA_STATUS_BIT_TIMEOUT 2u
 #define PA_STATUS_BIT_WORKSPACE 4u
+#define PA_STATUS_BIT_PLAN 8u /* pa_plan_device: a length breaks a constraint */
 
 /*
  * Problem description shared by pa_plan and pa_forward.
@@ -267,6 +268,62 @@ pa_status pa_forward_noalloc(const pa_config* cfg, const void* query, const void
                              const void* mask, const float* alibi_slopes, const int32_t* work,
                              int64_t n_items, const int32_t* combine, int64_t n_combine,
                              size_t workspace_bytes, uint32_t* status, void* out, void* stream);
+
+/*
+ * Planning on the device. The work list depends on the context lengths, which
+ * change every decode step; pa_plan needs them on the host. The three calls
+ * below keep the whole step on the GPU instead: pa_plan_device builds the
+ * same lists as pa_plan (bit for bit, same rule) from device-resident
+ * lengths, and pa_forward_device_plan launches grids sized by the list
+ * capacities, whose CTAs past the device-side counts return at once. The
+ * launches of a step then no longer depend on the lengths, so a caller can
+ * record plan + forward once (e.g. as a CUDA graph, the analogue of the
+ * graph-launch mode the operator pages mention for their metadata operator)
+ * and replay it after updating the lengths in place.
+ *
+ * pa_plan_bounds (host): capacities that hold the lists of any lengths the
+ *   configuration admits, and a workspace size that holds their partial
+ *   rows. With tiles T = batch * Hk * ceil(G * max_seqlen_q / TR):
+ *   comb_cap = T; work_cap = T * ceil(max_blocks_per_seq / chunk_blocks) for
+ *   an explicit chunk, else 8 * num_sms + T (the automatic chunk is at least
+ *   W / (8 * num_sms)); workspace for work_cap * TR partial rows.
+ */
+pa_status pa_plan_bounds(const pa_config* cfg, int64_t* work_cap, int64_t* comb_cap,
+                         size_t* workspace_bytes);
+
+/*
+ * pa_plan_device -- pa_plan on the GPU (asynchronous, one small kernel).
+ *
+ * context_lens, q_seqlens  device int32 [batch] (q_seqlens may be NULL)
+ * work, combine  device int32 [work_cap * PA_WORK_INTS], [comb_cap * PA_COMBINE_INTS]
+ * counts         device int32 [PA_PLAN_COUNTS]: items, combine entries,
+ *                partial rows, error (0 ok, 1 a length breaks a constraint, 2
+ *                a capacity is too small)
+ * workspace      the workspace of the forward pass that follows; on an error
+ *                the kernel sets PA_STATUS_BIT_PLAN (lengths) or
+ *                PA_STATUS_BIT_WORKSPACE (capacity) in its status word and
+ *                writes zero counts, so the forward pass does nothing.
+ * Host-side checks (configuration, pointers) return before any launch.
+ */
+#define PA_PLAN_COUNTS 4
+pa_status pa_plan_device(const pa_config* cfg, const int32_t* context_lens,
+                         const int32_t* q_seqlens, int32_t* work, int64_t work_cap,
+                         int32_t* combine, int64_t comb_cap, int32_t* counts, void* workspace,
+                         void* stream);
+
+/*
+ * pa_forward_device_plan -- pa_forward over the lists of pa_plan_device.
+ * Arguments as pa_forward, with the capacities in place of the list lengths
+ * and `counts` the planner's device counts. Launches work_cap attention CTAs
+ * and comb_cap combine CTAs whatever the counts.
+ */
+pa_status pa_forward_device_plan(const pa_config* cfg, const void* query, const void* key_cache,
+                                 const void* value_cache, const int32_t* block_tables,
+                                 const int32_t* context_lens, const int32_t* q_seqlens,
+                                 const void* mask, const float* alibi_slopes,
+                                 const int32_t* work, int64_t work_cap, const int32_t* combine,
+                                 int64_t comb_cap, const int32_t* counts, void* workspace,
+                                 size_t workspace_bytes, void* out, void* stream);
 
 /* Zero the status word of a workspace (enqueued on stream). */
 pa_status pa_status_clear(void* workspace, void* stream);

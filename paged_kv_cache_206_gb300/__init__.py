@@ -37,8 +37,9 @@ PA_FMA_MAX_ROWS = 8
 PA_TC_TILE_ROWS = 64
 
 # Every symbol include/pa.h declares.
-EXPORTS = ("pa_plan", "pa_forward", "pa_forward_noalloc", "pa_status_clear", "pa_status_read",
-           "pa_status_string")
+EXPORTS = ("pa_plan", "pa_forward", "pa_forward_noalloc", "pa_plan_bounds", "pa_plan_device",
+           "pa_forward_device_plan", "pa_status_clear", "pa_status_read", "pa_status_string")
+PA_PLAN_COUNTS = 4
 
 # Size of the device array pa_forward_noalloc uses as its workspace.
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -91,6 +92,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.pa_forward.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, i64, P, i64, P, sz, P, P]
     lib.pa_forward_noalloc.restype = ctypes.c_int
     lib.pa_forward_noalloc.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, i64, P, i64, sz, P, P, P]
+    lib.pa_plan_bounds.restype = ctypes.c_int
+    lib.pa_plan_bounds.argtypes = [cfgp, P, P, P]
+    lib.pa_plan_device.restype = ctypes.c_int
+    lib.pa_plan_device.argtypes = [cfgp, P, P, P, i64, P, i64, P, P, P]
+    lib.pa_forward_device_plan.restype = ctypes.c_int
+    lib.pa_forward_device_plan.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, i64, P, i64, P, P, sz,
+                                           P, P]
     lib.pa_status_clear.restype = ctypes.c_int
     lib.pa_status_clear.argtypes = [P, P]
     lib.pa_status_read.restype = ctypes.c_int
@@ -377,6 +385,58 @@ class HostStep:
         with torch.cuda.stream(s):
             self.out.copy_(self.d_out, non_blocking=True)
         s.synchronize()
+        return self.out
+
+    def status(self, stream=None):
+        return pa_status_read(self.workspace, stream)
+
+
+def pa_plan_bounds(cfg: pa_config) -> tuple[int, int, int]:
+    """(work_cap, comb_cap, workspace_bytes) that hold any plan of ``cfg``."""
+    w, c, ws = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_size_t()
+    _check(load_library().pa_plan_bounds(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(c),
+                                         ctypes.byref(ws)), "pa_plan_bounds")
+    return w.value, c.value, ws.value
+
+
+class DevicePlanStep:
+    """A decode step planned on the device: pa_plan_device, then
+    pa_forward_device_plan, both on device tensors, with list buffers sized by
+    pa_plan_bounds. The launches do not depend on the lengths, so ``run`` may
+    be recorded in a CUDA graph and replayed after ``context_lens`` (and
+    ``q_seqlens``) are updated in place."""
+
+    def __init__(self, db: "DeviceBatch"):
+        import torch
+        self.db = db
+        dev = db.key_cache.device
+        self.work_cap, self.comb_cap, ws = pa_plan_bounds(db.cfg)
+        self.work = torch.zeros((self.work_cap, PA_WORK_INTS), dtype=torch.int32, device=dev)
+        self.combine = torch.zeros((max(self.comb_cap, 1), PA_COMBINE_INTS), dtype=torch.int32,
+                                   device=dev)
+        self.counts = torch.zeros(PA_PLAN_COUNTS, dtype=torch.int32, device=dev)
+        self.workspace = torch.zeros(max(ws, PA_STATUS_BYTES), dtype=torch.uint8, device=dev)
+        self.out = torch.empty_like(db.out)
+
+    def plan(self, stream=None):
+        db = self.db
+        _check(load_library().pa_plan_device(
+            ctypes.byref(db.cfg), _tptr(db.context_lens), _tptr(db.q_seqlens), _tptr(self.work),
+            self.work_cap, _tptr(self.combine), self.comb_cap, _tptr(self.counts),
+            _tptr(self.workspace), _stream_handle(stream)), "pa_plan_device")
+
+    def forward(self, stream=None):
+        db = self.db
+        _check(load_library().pa_forward_device_plan(
+            ctypes.byref(db.cfg), _tptr(db.query), _tptr(db.key_cache), _tptr(db.value_cache),
+            _tptr(db.block_tables), _tptr(db.context_lens), _tptr(db.q_seqlens), _tptr(db.mask),
+            _tptr(db.alibi_slopes), _tptr(self.work), self.work_cap, _tptr(self.combine),
+            self.comb_cap, _tptr(self.counts), _tptr(self.workspace), self.workspace.numel(),
+            _tptr(self.out), _stream_handle(stream)), "pa_forward_device_plan")
+
+    def run(self, stream=None):
+        self.plan(stream)
+        self.forward(stream)
         return self.out
 
     def status(self, stream=None):

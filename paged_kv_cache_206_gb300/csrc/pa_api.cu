@@ -14,6 +14,7 @@
 #include "pa_decode_tc.cuh"
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_plan_device.h"
 
 namespace pa {
 
@@ -159,13 +160,18 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 }  // namespace
 }  // namespace pa
 
-extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const void* key_cache,
-                                const void* value_cache, const int32_t* block_tables,
-                                const int32_t* context_lens, const int32_t* q_seqlens,
-                                const void* mask, const float* alibi_slopes, const int32_t* work,
-                                int64_t n_items, const int32_t* combine, int64_t n_combine,
-                                void* workspace, size_t workspace_bytes, void* out,
-                                void* stream_) {
+namespace {
+
+// The forward pass. With `counts` null the grids are n_items and n_combine
+// CTAs; with a device plan they are the list capacities, and the CTAs past
+// the device-side counts (counts[0] items, counts[1] combine entries) return
+// at once.
+pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_cache,
+                       const void* value_cache, const int32_t* block_tables,
+                       const int32_t* context_lens, const int32_t* q_seqlens, const void* mask,
+                       const float* alibi_slopes, const int32_t* work, int64_t n_items,
+                       const int32_t* combine, int64_t n_combine, const int32_t* counts,
+                       void* workspace, size_t workspace_bytes, void* out, void* stream_) {
   using namespace pa;
   pa_status st = validate_config(cfg);
   if (st != PA_OK) return st;
@@ -217,6 +223,7 @@ extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const v
   P.num_blocks = c.num_blocks;
   P.mask_type = c.mask_type;
   P.kv_shared = kv_shared ? 1 : 0;
+  P.counts = counts;
   P.mask_q = int(max_q(c));
   P.mask_kv = int64_t(c.max_blocks_per_seq) * c.block_size;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / std::sqrt(float(hk));
@@ -265,9 +272,91 @@ extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const v
     C.num_heads = c.num_heads;
     C.group = P.group;
     C.hv = hv;
+    C.counts = counts;
     if (launch_combine(C, n_combine, int(TR), stream) != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_forward(const pa_config* cfg, const void* query, const void* key_cache,
+                                const void* value_cache, const int32_t* block_tables,
+                                const int32_t* context_lens, const int32_t* q_seqlens,
+                                const void* mask, const float* alibi_slopes, const int32_t* work,
+                                int64_t n_items, const int32_t* combine, int64_t n_combine,
+                                void* workspace, size_t workspace_bytes, void* out,
+                                void* stream) {
+  return forward_impl(cfg, query, key_cache, value_cache, block_tables, context_lens, q_seqlens,
+                      mask, alibi_slopes, work, n_items, combine, n_combine, nullptr, workspace,
+                      workspace_bytes, out, stream);
+}
+
+extern "C" pa_status pa_plan_bounds(const pa_config* cfg, int64_t* work_cap, int64_t* comb_cap,
+                                    size_t* workspace_bytes) {
+  using namespace pa;
+  const pa_status st = validate_config(cfg);
+  if (st != PA_OK) return st;
+  const pa_config& c = *cfg;
+  const int64_t TR = tile_rows(c);
+  const int64_t rows = int64_t(c.num_heads / c.kv_heads) * max_q(c);
+  const int64_t tiles = int64_t(c.batch) * c.kv_heads * cdiv(rows, TR);
+  const int64_t items = c.chunk_blocks > 0 ? tiles * cdiv(c.max_blocks_per_seq, c.chunk_blocks)
+                                           : 8 * int64_t(c.num_sms) + tiles;
+  if (items > INT32_MAX || items * TR > INT32_MAX) return PA_ERR_INVALID_ARG;
+  if (work_cap) *work_cap = items;
+  if (comb_cap) *comb_cap = tiles;
+  if (workspace_bytes) *workspace_bytes = workspace_layout(items * TR, c.head_size_v).total;
+  return PA_OK;
+}
+
+extern "C" pa_status pa_plan_device(const pa_config* cfg, const int32_t* context_lens,
+                                    const int32_t* q_seqlens, int32_t* work, int64_t work_cap,
+                                    int32_t* combine, int64_t comb_cap, int32_t* counts,
+                                    void* workspace, void* stream) {
+  using namespace pa;
+  const pa_status st = validate_config(cfg);
+  if (st != PA_OK) return st;
+  const pa_config& c = *cfg;
+  if (!context_lens || !work || !counts || !workspace || (comb_cap > 0 && !combine))
+    return PA_ERR_INVALID_ARG;
+  if (work_cap < 1 || comb_cap < 0 || work_cap > INT32_MAX || comb_cap > INT32_MAX)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+  DevPlanParams D{};
+  D.context_lens = context_lens;
+  D.q_seqlens = q_seqlens;
+  D.work = work;
+  D.combine = combine;
+  D.counts = counts;
+  D.status = static_cast<uint32_t*>(workspace);
+  D.work_cap = work_cap;
+  D.comb_cap = comb_cap;
+  D.batch = c.batch;
+  D.num_heads = c.num_heads;
+  D.kv_heads = c.kv_heads;
+  D.group = c.num_heads / c.kv_heads;
+  D.block_size = c.block_size;
+  D.max_blocks_per_seq = c.max_blocks_per_seq;
+  D.maxq = int(max_q(c));
+  D.tr = int(tile_rows(c));
+  D.chunk_blocks = c.chunk_blocks;
+  D.num_sms = c.num_sms;
+  D.hk = c.head_size_k;
+  D.hv = c.head_size_v;
+  return launch_plan(D, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status pa_forward_device_plan(
+    const pa_config* cfg, const void* query, const void* key_cache, const void* value_cache,
+    const int32_t* block_tables, const int32_t* context_lens, const int32_t* q_seqlens,
+    const void* mask, const float* alibi_slopes, const int32_t* work, int64_t work_cap,
+    const int32_t* combine, int64_t comb_cap, const int32_t* counts, void* workspace,
+    size_t workspace_bytes, void* out, void* stream) {
+  if (!counts || work_cap < 1) return PA_ERR_INVALID_ARG;
+  return forward_impl(cfg, query, key_cache, value_cache, block_tables, context_lens, q_seqlens,
+                      mask, alibi_slopes, work, work_cap, combine, comb_cap, counts, workspace,
+                      workspace_bytes, out, stream);
 }
 
 extern "C" pa_status pa_status_clear(void* workspace, void* stream) {
@@ -289,6 +378,7 @@ extern "C" pa_status pa_status_read(const void* workspace, void* stream_, uint32
   if (v & PA_STATUS_BIT_TIMEOUT) return PA_ERR_TIMEOUT;
   if (v & PA_STATUS_BIT_BLOCK_INDEX) return PA_ERR_BLOCK_INDEX;
   if (v & PA_STATUS_BIT_WORKSPACE) return PA_ERR_BUFFER_TOO_SMALL;
+  if (v & PA_STATUS_BIT_PLAN) return PA_ERR_INVALID_ARG;
   return PA_OK;
 }
 

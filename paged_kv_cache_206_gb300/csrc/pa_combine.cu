@@ -12,6 +12,7 @@ namespace pa {
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams C) {
   __shared__ float wts[kCombineThreads / 32][kCombineMaxSplits];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (C.counts && int(blockIdx.x) >= C.counts[1]) return;
   // Launched as a programmatic dependent of the attention kernel: wait until
   // that grid has finished and its partial results are visible.
   grid_dependency_wait();

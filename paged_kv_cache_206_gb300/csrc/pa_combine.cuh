@@ -21,6 +21,7 @@ struct CombineParams {
   uint32_t* status;
   int64_t part_rows_cap;
   int num_heads, group, hv;
+  const int32_t* counts;  // device plan: counts[1] combine entries (CTAs past it exit), else null
 };
 
 cudaError_t launch_combine(const CombineParams& C, int64_t n_combine, int tile_rows,

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(128) fma_decode_kernel(const __grid_constant__
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, NW = blockDim.x >> 5;
   constexpr unsigned FULL = 0xffffffffu;
 
+  if (P.counts && int(blockIdx.x) >= P.counts[0]) return;  // past a device plan's items
   Item it;
   it.load(P, blockIdx.x);
   const int hk = P.hk, hv = P.hv, G = P.group;

@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(128) mma_decode_kernel(const __grid_constant__
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, NW = blockDim.x >> 5;
   const int g = lane >> 2, c = lane & 3;
 
+  if (P.counts && int(blockIdx.x) >= P.counts[0]) return;  // past a device plan's items
   Item it;
   it.load(P, blockIdx.x);
   const int G = P.group;

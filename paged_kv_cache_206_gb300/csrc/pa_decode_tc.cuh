@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   uint64_t* o_done = s_full + 9;          // every PV MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.tmem_slot_off);
 
+  if (P.counts && int(blockIdx.x) >= P.counts[0]) return;  // past a device plan's items
   Item it;
   it.load(P, blockIdx.x);
   const int G = P.group, bs = P.block_size;

@@ -159,6 +159,7 @@ struct FwdParams {
   const __half* mask;        // may be null
   const float* alibi_slopes; // may be null
   const int32_t* work;
+  const int32_t* counts;  // device plan: counts[0] items (CTAs past it exit), else null
   __half* out;
   uint32_t* status;
   float* part_o;

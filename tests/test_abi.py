@@ -100,4 +100,35 @@ def test_forward_host_checks(lib):
     other = ctypes.c_void_p((1 << 21))
     assert _fwd(lib, wide_v, value=other, n_items=0, work=None) == pa.PA_OK
     assert lib.pa_status_clear(None, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_plan_bounds_and_device_plan_host_checks(lib):
+    import numpy as np
+    for kw in (dict(), dict(max_seqlen_q=3, num_heads=16, kv_heads=1), dict(chunk_blocks=3),
+               dict(batch=7, max_blocks_per_seq=40, num_sms=152)):
+        c = _cfg(**kw)
+        w, m, ws = pa.pa_plan_bounds(c)
+        assert (w, m) == pa.list_capacity(c)
+        rows = (c.num_heads // c.kv_heads) * max(1, c.max_seqlen_q)
+        tr = rows if rows <= 8 else 64
+        up = lambda x: (x + 255) // 256 * 256
+        assert ws == up(up(256 + w * tr * c.head_size_v * 4) + w * tr * 4)
+    fake = ctypes.c_void_p(1 << 20)
+    c = _cfg()
+
+    def dev(cfg, **kw):
+        a = dict(ctx=fake, ql=None, work=fake, wcap=4, comb=fake, ccap=4, counts=fake, ws=fake)
+        a.update(kw)
+        return lib.pa_plan_device(ctypes.byref(cfg), a["ctx"], a["ql"], a["work"], a["wcap"],
+                                  a["comb"], a["ccap"], a["counts"], a["ws"], None)
+    assert dev(c, ctx=None) == pa.PA_ERR_INVALID_ARG
+    assert dev(c, counts=None) == pa.PA_ERR_INVALID_ARG
+    assert dev(c, wcap=0) == pa.PA_ERR_INVALID_ARG
+    assert dev(c, comb=None) == pa.PA_ERR_INVALID_ARG
+    assert dev(c, ws=ctypes.c_void_p((1 << 20) + 64)) == pa.PA_ERR_INVALID_ARG
+    assert dev(_cfg(block_size=8)) == pa.PA_ERR_INVALID_ARG
+    assert dev(_cfg(mask_type=4)) == pa.PA_ERR_UNSUPPORTED
+    assert lib.pa_forward_device_plan(ctypes.byref(c), fake, fake, fake, fake, fake, None, None,
+                                      None, fake, 4, None, 0, None, fake, 256, fake,
+                                      None) == pa.PA_ERR_INVALID_ARG  # counts required
     assert lib.pa_status_read(None, None, None) == pa.PA_ERR_INVALID_ARG
