@@ -148,7 +148,8 @@ typedef struct pa_config {
  * Otherwise
  *   W     = sum_b NB_b * Hk * QT_b
  *   c_bal = ceil(W / (8 * num_sms))
- *   c_min = ceil(64 * TR * hv / (bs * (hk + hv)))
+ *   RT    = min(TR, G * max_seqlen_q)   (rows a full tile really holds)
+ *   c_min = ceil(64 * RT * hv / (bs * (hk + hv)))
  *   c     = max(1, c_bal, c_min)
  * (c_bal aims at about eight work items per SM so that variable lengths
  * balance; c_min keeps the partial results that a split writes and re-reads

@@ -87,7 +87,8 @@ extern "C" pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens,
     chunk = c.chunk_blocks;
   } else {
     const int64_t bal = cdiv(W, 8 * int64_t(c.num_sms));
-    const int64_t lo = cdiv(64 * TR * c.head_size_v, bs * (c.head_size_k + c.head_size_v));
+    const int64_t RT = std::min(TR, G * maxq);  // rows a full tile really holds
+    const int64_t lo = cdiv(64 * RT * c.head_size_v, bs * (c.head_size_k + c.head_size_v));
     chunk = std::max<int64_t>(1, std::max(bal, lo));
   }
 

@@ -117,6 +117,12 @@ def test_auto_chunk_rule_values(lib):
             max_blocks_per_seq=32, num_sms=152)
     p = pa.pa_plan(c, np.full(64, 4096, np.int32))
     assert sorted(set((p.work[:, 5] - p.work[:, 4]).tolist())) == [4, 14]
+    # c_min counts the rows a tile really holds: 16 heads on one kv head fill
+    # 16 of the 64 rows -> ceil(64*16*512 / (64*(576+512))) = ceil(7.53) = 8
+    c = cfg(batch=8, num_heads=16, kv_heads=1, head_size_k=576, head_size_v=512,
+            block_size=64, max_blocks_per_seq=128, num_sms=152)
+    p = pa.pa_plan(c, np.full(8, 8192, np.int32))
+    assert set((p.work[:, 5] - p.work[:, 4]).tolist()) == {8}
 
 
 def test_two_call_convention_and_small_buffers(lib):
