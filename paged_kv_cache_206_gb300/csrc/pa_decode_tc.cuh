@@ -64,6 +64,8 @@ constexpr int kTcRows = PA_TC_TILE_ROWS;  // N of both MMAs (query rows, padded)
 constexpr int kTcTok = 64;                // tokens per tile (M of QK^T)
 constexpr int kTcKSlots = 3;              // K ring of 16 KB boxes
 constexpr int kTcVSlots = 5;              // V ring of 16 KB boxes
+constexpr int kTcPBufs = 2;               // P^T buffers (softmax of tile n + kTcPBufs
+                                          // waits for the PV of tile n)
 constexpr uint32_t kTcHalfBytes = kTcTok * 128;      // 64 tokens x 64 dims x 2 B
 constexpr uint32_t kTcSlotBytes = 2 * kTcHalfBytes;  // 64 tokens x 128 dims
 constexpr int kTcThreads = 384;  // 2 producers, 2 MMA issuers, 8 softmax warps
@@ -76,8 +78,8 @@ struct TcLayout {
 __host__ __device__ inline TcLayout tc_layout(int hk) {
   TcLayout L;
   L.q_off = 0;                                            // [hk/64][64 rows][128 B]
-  L.p_off = L.q_off + uint32_t(hk / 64) * kTcRows * 128;  // 2 x [64 tok][64 rows] fp16
-  L.ring_off = L.p_off + 2 * kTcTok * 128;                // K ring, then V ring
+  L.p_off = L.q_off + uint32_t(hk / 64) * kTcRows * 128;  // kTcPBufs x [64 tok][64 rows] fp16
+  L.ring_off = L.p_off + kTcPBufs * kTcTok * 128;         // K ring, then V ring
   L.red_off = L.ring_off + (kTcKSlots + kTcVSlots) * kTcSlotBytes;  // [4][64] fp32 exchange
   L.rows_off = L.red_off + 4 * kTcRows * 4;               // per-row constants
   L.bars_off = L.rows_off + 6 * kTcRows * 4;              // mbarriers
@@ -458,7 +460,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const uint32_t p_addr = smem_u32(p_s), ring_addr = smem_u32(vring);
     int consumed = 0;
     for (int n = 0; n < ntiles && ok; ++n) {
-      if (!warp_wait(&p_full[n & 1], (n >> 1) & 1, lane)) { ok = false; break; }
+      const int pb = n % kTcPBufs;
+      if (!warp_wait(&p_full[pb], (n / kTcPBufs) & 1, lane)) { ok = false; break; }
       tc_fence_after();
       const int nvalid = min(kTcTok, it.tok1 - (it.tok0 + n * kTcTok));
       for (int oc = 0; oc < VS; ++oc, ++consumed) {
@@ -481,7 +484,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
 #pragma unroll
           for (int k = 0; k < kTcTok / 16; ++k) {
             const uint64_t a = smem_desc(ring_addr + slot * kTcSlotBytes + k * 2048, kTcHalfBytes, 1024);
-            const uint64_t b = smem_desc(p_addr + (n & 1) * (kTcTok * 128) + k * 2048, kTcHalfBytes, 1024);
+            const uint64_t b = smem_desc(p_addr + pb * (kTcTok * 128) + k * 2048, kTcHalfBytes, 1024);
             tc_mma(tmem_o + oc * 64, a, b, kIdescPV, (n | k) != 0);
           }
           tc_commit(&vempty[slot]);
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(&pv_done[n & 1]);
+      if (lane == 0) tc_commit(&pv_done[pb]);
       __syncwarp();
     }
     if (!ok && lane == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
@@ -599,12 +602,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       }
 #pragma unroll
       for (int r = 0; r < 32; ++r) l_t[r] += s[r];
-      // P^T buffer n & 1 was last read by PV(n - 2); a rescale of O^T also
-      // needs PV(n - 1). Each wait is on the barrier of that PV's P^T buffer.
+      // P^T buffer n % kTcPBufs was last read by PV(n - kTcPBufs); a rescale
+      // of O^T also needs PV(n - 1). Each wait is on the barrier of that PV's
+      // P^T buffer, whose next phase needs P^T(n) and so cannot have begun.
       {
         bool pv = true;
-        if (grew && n >= 1) pv = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1);
-        if (n >= 2) pv = pv && mbar_wait(&pv_done[n & 1], ((n - 2) >> 1) & 1);
+        if (grew && n >= 1)
+          pv = mbar_wait(&pv_done[(n - 1) % kTcPBufs], ((n - 1) / kTcPBufs) & 1);
+        if (n >= kTcPBufs)
+          pv = pv && mbar_wait(&pv_done[n % kTcPBufs], ((n - kTcPBufs) / kTcPBufs) & 1);
         if (softmax_bar_or(!pv)) { ok = false; break; }
         tc_fence_after();
       }
@@ -619,7 +625,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
           pk.z = pack_half2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
           pk.w = pack_half2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
           const int chunk = 4 * rh + c8;
-          *reinterpret_cast<uint4*>(p_s + (n & 1) * (kTcTok * 128) + tt * 128 + ((chunk ^ (tt & 7)) << 4)) = pk;
+          *reinterpret_cast<uint4*>(p_s + (n % kTcPBufs) * (kTcTok * 128) + tt * 128 + ((chunk ^ (tt & 7)) << 4)) = pk;
         }
       }
       if (grew) {
@@ -640,7 +646,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       fence_proxy_async();  // P^T is read by the tensor cores
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[n & 1]);
+      if (lane == 0) mbar_arrive(&p_full[n % kTcPBufs]);
     }
     const int t = quarter * 32 + lane;  // TMEM lane of this thread = output dim in a chunk
     if (!ok && t == 0 && rh == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
