@@ -38,6 +38,7 @@ METRIC = "paged-attn effective KV HBM GB/s (% of GB300 peak) and query tokens/s"
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_TFLOPS = 1900.0
 FLUSH_BYTES = 512 << 20
 
 
@@ -55,11 +56,14 @@ def parse():
 
 
 def peaks():
+    """(HBM GB/s, dense fp16/bf16 tensor TFLOP/s burst, 'measured' | 'fallback').
+    fp16 and bf16 run at the same nominal tensor rate, so the measured bf16
+    GEMM figure serves fp16 with ratio 1."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_TFLOPS)), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_TFLOPS, "fallback"
 
 
 # Device sources of each attention kernel: an ncu figure stays valid while
@@ -212,7 +216,8 @@ def cpu_baseline(w, max_seconds=20.0):
     t0 = time.perf_counter()
     _, used = oracle.attention(w, subset=sub, threads=cores)
     dt = time.perf_counter() - t0
-    kv = int(w.context_lens[sub].astype(np.int64).sum()) * w.kv_heads * (w.head_size_k + w.head_size_v) * 2
+    per = w.head_size_k + (0 if w.shared_kv else w.head_size_v)
+    kv = int(w.context_lens[sub].astype(np.int64).sum()) * w.kv_heads * per * 2
     return {"value": kv / dt / 1e9, "unit": UNIT, "cores": int(used), "kind": "oracle",
             "seconds": dt,
             "sample": f"{n} of {w.batch} sequences ({kv / 1e9:.3f} GB of KV), fp64 C oracle, "
@@ -233,7 +238,8 @@ def run_reference(args):
     one = max(time.perf_counter() - t0, 1e-4)
     n = max(1, min(w.batch, int(0.5 * min(cores, w.batch) / one)))
     sub = list(range(n))
-    kv = int(w.context_lens[sub].astype(np.int64).sum()) * w.kv_heads * (w.head_size_k + w.head_size_v) * 2
+    per = w.head_size_k + (0 if w.shared_kv else w.head_size_v)
+    kv = int(w.context_lens[sub].astype(np.int64).sum()) * w.kv_heads * per * 2
     used = 1
     for _ in range(args.warmup):
         _, used = oracle.attention(w, subset=sub, threads=cores)
@@ -374,9 +380,20 @@ def main():
             dist.destroy_process_group()
         return
 
-    peak, peak_kind = peaks()
+    peak, tpeak, peak_kind = peaks()
     value = kv_all / (ms * 1e-3) / 1e9
     achieved = (kv_bytes + qo_bytes) / (dec_ms * 1e-3) / 1e9
+    flops = w.attn_flops()
+    # the bound: tensor when the arithmetic intensity passes the ridge point
+    tensor_bound = flops / (kv_bytes + qo_bytes) > tpeak * 1e3 / peak
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": flops / (dec_ms * 1e-3) / 1e12, "peak": tpeak,
+                "unit": "TFLOP/s", "flops": flops,
+                "bytes": "2*(hk+hv) flop per (query row, visible key), algorithmic"}
+    else:
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "bytes": "KV + Q + O per launch (algorithmic)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
     kernel = dominant_kernel(db.cfg)
     traffic = ncu_traffic(kernel, args.workload)
     base = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w)
@@ -404,12 +421,8 @@ def main():
         },
         "query_tokens_per_s": q_all / (ms * 1e-3),
         "pct_of_nominal_8tbs": 100.0 * value / NOMINAL_HBM_GBS,
-        "roofline": {
-            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-            "kernel": kernel,
-            "bytes": "KV + Q + O per launch (algorithmic)", "kernel_ms": dec_ms,
-        },
+        "roofline": dict(roof, traffic=traffic, peak_kind=peak_kind, kernel=kernel,
+                         kernel_ms=dec_ms),
         "e2e": None if not e2e_t else {
             "value": kv_all / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3},

@@ -62,10 +62,11 @@ namespace pa {
 
 constexpr int kTcRows = PA_TC_TILE_ROWS;  // N of both MMAs (query rows, padded)
 constexpr int kTcTok = 64;                // tokens per tile (M of QK^T)
-constexpr int kTcKSlots = 3;              // K ring of 16 KB boxes
-constexpr int kTcVSlots = 5;              // V ring of 16 KB boxes
-constexpr int kTcPBufs = 2;               // P^T buffers (softmax of tile n + kTcPBufs
+constexpr int kTcKSlots = 4;              // K ring of 16 KB boxes
+constexpr int kTcVSlots = 4;              // V ring of 16 KB boxes
+constexpr int kTcPBufs = 1;               // P^T buffers (softmax of tile n + kTcPBufs
                                           // waits for the PV of tile n)
+constexpr int kTcPrefetchTiles = 0;       // L2 prefetch distance of the producers (tiles)
 constexpr uint32_t kTcHalfBytes = kTcTok * 128;      // 64 tokens x 64 dims x 2 B
 constexpr uint32_t kTcSlotBytes = 2 * kTcHalfBytes;  // 64 tokens x 128 dims
 constexpr int kTcThreads = 384;  // 2 producers, 2 MMA issuers, 8 softmax warps
@@ -268,9 +269,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   Item it;
   it.load(P, blockIdx.x);
   const int G = P.group, bs = P.block_size;
+  const int prefix = it.L - it.qlen;
+  if (P.mask_type == PA_MASK_NORM_COMPRESS && it.nrows > 0) {
+    // Causal trim: keys past the position of the tile's last query token are
+    // masked (a large negative fill) for every row of the tile, so their
+    // probabilities are exactly zero in fp32; the item stops before them.
+    // Prefill tiles (q = L) thus skip the upper triangle; a split that lies
+    // wholly past it becomes empty (never split 0, which starts at key 0).
+    const int pmax = prefix + (it.r0 + it.nrows - 1) / G;
+    it.tok1 = max(it.tok0, min(it.tok1, pmax + 1));
+  }
   const int ntok = it.tok1 - it.tok0;
   const int ntiles = ntok > 0 ? (ntok + kTcTok - 1) / kTcTok : 0;
-  const int prefix = it.L - it.qlen;
   const int sigma = it.L > PA_COMPRESS_MASK_SIZE ? it.L - PA_COMPRESS_MASK_SIZE : 0;
 
   // ---- set-up: barriers, TMEM, query tile, per-row constants
@@ -359,7 +369,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       const int pieces = kTcTok / box_rows;
       int issued = 0;
       bool ok = true;
+      // L2 prefetch of tile m's boxes (valid block-table entries only)
+      auto prefetch_tile = [&](int m) {
+        const int t0 = it.tok0 + m * kTcTok;
+        for (int pc = 0; pc < pieces; ++pc) {
+          const int tok = t0 + pc * box_rows;
+          if (tok >= it.tok1) break;
+          const int phys = bt_row[tok / bs];
+          if (phys < 0 || phys >= P.num_blocks) continue;
+          const int row = phys * bs + tok % bs;
+          for (int sl = 0; sl < per_tile; ++sl) {
+            tma_prefetch_3d(map, 0, row, zbase + 2 * sl);
+            if (box_rows != kTcTok && !(is_k && (KH & 1) && sl == KS - 1))
+              tma_prefetch_3d(map, 0, row, zbase + 2 * sl + 1);
+          }
+        }
+      };
+      if (kTcPrefetchTiles > 0)
+        for (int m = 1; m <= kTcPrefetchTiles && m < ntiles; ++m) prefetch_tile(m);
       for (int n = 0; n < ntiles && ok; ++n) {
+        if (kTcPrefetchTiles > 0 && n > 0 && n + kTcPrefetchTiles < ntiles)
+          prefetch_tile(n + kTcPrefetchTiles);
         // physical rows of the tile's pieces (-1: past the range or a bad entry)
         const int t0 = it.tok0 + n * kTcTok;
         int ph[4], rws[4];
@@ -690,6 +720,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
             if (d == 0) P.part_lse[it.slot + r] = (m_used[r] + log2f(l_tot[r])) * kLn2;
           }
         }
+      }
+    } else if (done && it.slot >= 0 && int64_t(it.slot) + it.nrows <= P.part_rows_cap) {
+      // an empty split (causal trim): weight zero in the combine
+      for (int idx = t + 128 * rh; idx < it.nrows * HV; idx += 256) {
+        P.part_o[int64_t(it.slot) * HV + idx] = 0.f;
+        if (idx % HV == 0) P.part_lse[it.slot + idx / HV] = -INFINITY;
       }
     }
   }

@@ -83,6 +83,18 @@ class Workload:
         per = self.head_size_k + (0 if self.shared_kv else self.head_size_v)
         return int(self.context_lens.astype(np.int64).sum()) * self.kv_heads * per * 2
 
+    def attn_flops(self) -> int:
+        """Multiply-add flops of QK^T and PV over the keys each query row sees:
+        2 * (hk + hv) per (row, key); with the causal mask row i of a sequence
+        sees L - q + i + 1 keys, otherwise all L."""
+        L = self.context_lens.astype(np.int64)
+        q = self.q_seqlens.astype(np.int64)
+        if self.mask_type == MASK_NORM_COMPRESS:
+            pairs = (q * (L - q) + q * (q + 1) // 2).sum()
+        else:
+            pairs = (q * L).sum()
+        return int(pairs) * self.num_heads * 2 * (self.head_size_k + self.head_size_v)
+
     def qo_bytes(self) -> int:
         """Bytes of query read plus output written (fp16)."""
         return self.total_q * self.num_heads * (self.head_size_k + self.head_size_v) * 2
@@ -313,6 +325,14 @@ def mla_decode(seed: int = 0, batch: int = 64, max_len: int = 8192) -> Workload:
                          shared_kv=True)
 
 
+def prefill_causal(seed: int = 0, batch: int = 4, seq_len: int = 2048) -> Workload:
+    """Prefill over the paged cache (PA_ENCODER shape, q = L): B=4, H=Hk=32,
+    hk=128, bs=128, q = L = 2048, compressed causal mask with fill -10000."""
+    return make_workload("prefill_causal", context_lens=[seq_len] * batch, q_seqlens=seq_len,
+                         num_heads=32, kv_heads=32, head_size_k=128, block_size=128,
+                         mask_type=MASK_NORM_COMPRESS, seed=seed)
+
+
 NAMED = {
     "tiny_decode": tiny_decode,
     "gqa_decode": gqa_decode,
@@ -320,4 +340,5 @@ NAMED = {
     "alibi_decode": alibi_decode,
     "mqa_split": mqa_split,
     "mla_decode": mla_decode,
+    "prefill_causal": prefill_causal,
 }

@@ -195,6 +195,17 @@ TC_CASES = {
     # block_size 256: a tile is half a block
     "tc_bs256": lambda: W.make_workload("tc256", context_lens=[600, 256, 257], num_heads=16,
                                         kv_heads=1, head_size_k=128, block_size=256, seed=35),
+    # prefill (q = L) with the causal mask: 64-token row tiles skip the keys
+    # past their last token; 1-block chunks make splits that lie wholly past
+    # it (empty, weight zero in the combine)
+    "tc_prefill_split": lambda: W.make_workload("pf", context_lens=[300, 129], q_seqlens=[300, 129],
+                                                num_heads=2, kv_heads=2, head_size_k=128,
+                                                block_size=64, mask_type=W.MASK_NORM_COMPRESS,
+                                                seed=40, chunk_blocks=1),
+    "tc_prefill_gqa": lambda: W.make_workload("pfg", context_lens=[200, 77], q_seqlens=[200, 70],
+                                              num_heads=8, kv_heads=2, head_size_k=128,
+                                              block_size=32, mask_type=W.MASK_NORM_COMPRESS,
+                                              seed=41),
     # MASK_TYPE_NORM on the tensor-core path: 16 heads x 2 tokens per kv head
     "tc_norm": lambda: W.make_workload("tcn", context_lens=[300, 1200], q_seqlens=[2, 1],
                                        num_heads=16, kv_heads=1, head_size_k=128, block_size=64,

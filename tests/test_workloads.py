@@ -40,3 +40,12 @@ def test_norm_mask_layout_and_poison():
     assert m[0, 0, 4] == np.float16(-10000.0) and np.isfinite(m[0, 1, 4])
     assert np.isnan(m[0, :, 5:].astype(np.float32)).all()
     assert np.isnan(m[1, 1].astype(np.float32)).all()  # sequence 1 has one query token
+
+
+def test_attention_flops_count_the_visible_keys():
+    # causal: L=5, q=3 -> rows see 3, 4, 5 keys = 12 pairs; L=4, q=1 -> 4
+    w = W.make_workload("f", context_lens=[5, 4], q_seqlens=[3, 1], num_heads=2, kv_heads=1,
+                        head_size_k=16, block_size=16, mask_type=W.MASK_NORM_COMPRESS, seed=5)
+    assert w.attn_flops() == 16 * 2 * 2 * 32
+    w.mask_type = W.MASK_NONE  # every row sees all L keys: 3*5 + 4 = 19
+    assert w.attn_flops() == 19 * 2 * 2 * 32
