@@ -66,7 +66,6 @@ constexpr int kTcKSlots = 4;              // K ring of 16 KB boxes
 constexpr int kTcVSlots = 4;              // V ring of 16 KB boxes
 constexpr int kTcPBufs = 1;               // P^T buffers (softmax of tile n + kTcPBufs
                                           // waits for the PV of tile n)
-constexpr int kTcPrefetchTiles = 0;       // L2 prefetch distance of the producers (tiles)
 constexpr uint32_t kTcHalfBytes = kTcTok * 128;      // 64 tokens x 64 dims x 2 B
 constexpr uint32_t kTcSlotBytes = 2 * kTcHalfBytes;  // 64 tokens x 128 dims
 constexpr int kTcThreads = 384;  // 2 producers, 2 MMA issuers, 8 softmax warps
@@ -369,27 +368,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       const int pieces = kTcTok / box_rows;
       int issued = 0;
       bool ok = true;
-      // L2 prefetch of tile m's boxes (valid block-table entries only)
-      auto prefetch_tile = [&](int m) {
-        const int t0 = it.tok0 + m * kTcTok;
-        for (int pc = 0; pc < pieces; ++pc) {
-          const int tok = t0 + pc * box_rows;
-          if (tok >= it.tok1) break;
-          const int phys = bt_row[tok / bs];
-          if (phys < 0 || phys >= P.num_blocks) continue;
-          const int row = phys * bs + tok % bs;
-          for (int sl = 0; sl < per_tile; ++sl) {
-            tma_prefetch_3d(map, 0, row, zbase + 2 * sl);
-            if (box_rows != kTcTok && !(is_k && (KH & 1) && sl == KS - 1))
-              tma_prefetch_3d(map, 0, row, zbase + 2 * sl + 1);
-          }
-        }
-      };
-      if (kTcPrefetchTiles > 0)
-        for (int m = 1; m <= kTcPrefetchTiles && m < ntiles; ++m) prefetch_tile(m);
       for (int n = 0; n < ntiles && ok; ++n) {
-        if (kTcPrefetchTiles > 0 && n > 0 && n + kTcPrefetchTiles < ntiles)
-          prefetch_tile(n + kTcPrefetchTiles);
         // physical rows of the tile's pieces (-1: past the range or a bad entry)
         const int t0 = it.tok0 + n * kTcTok;
         int ph[4], rws[4];

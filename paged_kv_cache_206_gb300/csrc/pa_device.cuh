@@ -94,15 +94,6 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t 
                : "memory");
 }
 
-// Prefetch one 3-D tensor-map box into L2 (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t x, int32_t y,
-                                                int32_t z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
 // L2 policy for data read once per pass (the KV stream).
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
