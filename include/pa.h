@@ -35,9 +35,8 @@
  *                          the kernels read the entries with i < q_b and
  *                          j < L_b only.
  * The mask value is added to the scaled score, not substituted by -inf, and is
- * not scaled. The kernels read the mask only where j > L_b - q_b: every other
- * element they would read lies on or below the diagonal, which the pages fix
- * at 0.
+ * not scaled. The kernels read the compressed mask only above the diagonal
+ * (j > p): the pages fix the diagonal and the lower triangle at 0.
  *
  * The split-KV path follows SparseAttnSharedkvMetadata ("功能说明" and the
  * `metadata` output): a task list gives each CTA its (batch, head group, query

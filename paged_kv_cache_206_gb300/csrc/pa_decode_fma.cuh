@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(128) fma_decode_kernel(const __grid_constant__
       if (P.mask_type == PA_MASK_ALIBI) {
         x += slope2[rr] * float(j - prow[rr]);
       } else if (P.mask_type == PA_MASK_NORM_COMPRESS) {
-        if (tok_ok && j > prefix) {
+        if (tok_ok && j > prow[rr]) {  // above the diagonal only
           // both indices lie in [0, 2048) for a consistent plan; clamp anyway
           const int mr = min(max(prow[rr] - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
           const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);

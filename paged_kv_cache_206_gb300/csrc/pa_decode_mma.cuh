@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(128) mma_decode_kernel(const __grid_constant__
       if (P.mask_type == PA_MASK_ALIBI) {
         v += slope2[col] * float(j - prow[col]);
       } else if (P.mask_type == PA_MASK_NORM_COMPRESS) {
-        if (tok < nvalid && j > prefix) {
+        if (tok < nvalid && j > prow[col]) {  // above the diagonal only
           const int mr = min(max(prow[col] - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
           const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
           v += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;

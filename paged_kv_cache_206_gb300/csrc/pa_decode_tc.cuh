@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   uint64_t* pv_done = s_full + 6;         // [2] PV that read P^T buffer b complete
   uint64_t* qk_done = s_full + 8;         // every QK MMA complete
   uint64_t* o_done = s_full + 9;          // every PV MMA complete
+  uint64_t* q_ready = s_full + 10;        // query tile in shared memory (one arrival per softmax warp)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.tmem_slot_off);
 
   if (P.counts && int(blockIdx.x) >= P.counts[0]) return;  // past a device plan's items
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     }
     mbar_init(qk_done, 1);
     mbar_init(o_done, 1);
+    mbar_init(q_ready, 8);
     fence_barrier_init();
     flags[1] = 0;
   }
@@ -309,31 +311,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // Q tile: row r of the tile, chunk c (8 dims) -> box c/8, swizzled position.
-  // All of this thread's loads are issued before any store.
-  {
-    constexpr int kChunks = kTcRows * (HK / 8);
-    constexpr int kPer = (kChunks + kTcThreads - 1) / kTcThreads;
-    uint4 v[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int idx = tid + k * kTcThreads;
-      const int r = idx / (HK / 8), c = idx % (HK / 8);
-      v[k] = make_uint4(0, 0, 0, 0);
-      if (idx < kChunks && r < it.nrows) {
-        const int rr = it.r0 + r;
-        v[k] = *reinterpret_cast<const uint4*>(
-            P.query + (int64_t(it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G) * HK + c * 8);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int idx = tid + k * kTcThreads;
-      const int r = idx / (HK / 8), c = idx % (HK / 8);
-      if (idx < kChunks)
-        *reinterpret_cast<uint4*>(q_s + (c >> 3) * (kTcRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v[k];
-    }
-  }
   for (int r = tid; r < kTcRows; r += kTcThreads) {
     const bool ok = r < it.nrows;
     const int rr = it.r0 + r;
@@ -342,7 +319,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     m_used[r] = -INFINITY;
     l_tot[r] = 0.f;
   }
-  fence_proxy_async();  // query tile written by threads, read by the tensor cores
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -434,6 +410,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     bool ok = true;
     const uint32_t q_addr = smem_u32(q_s), ring_addr = smem_u32(kring);
     int consumed = 0;
+    // the softmax warps load the query tile while the producers already stream
+    if (ntiles > 0 && !warp_wait(q_ready, 0, lane)) ok = false;
     for (int m = 0; m < ntiles && ok; ++m) {
       if (m >= 2 && !warp_wait(&s_free[m & 1], ((m >> 1) - 1) & 1, lane)) { ok = false; break; }
       tc_fence_after();
@@ -509,6 +487,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     __syncwarp();
   } else {
     // ================= softmax warps 2-9 =================
+    // Query tile first (the producers are already streaming K and V): row r
+    // of the tile, chunk c (8 dims) -> box c/8, swizzled position, in two
+    // rounds whose loads are all issued before their stores.
+    {
+      const int st = tid - 64;  // 0..255
+      constexpr int kChunks = kTcRows * (HK / 8);
+      constexpr int kPer = (kChunks + 255) / 256;
+      constexpr int kHalf = (kPer + 1) / 2;
+#pragma unroll
+      for (int round = 0; round < 2; ++round) {
+        uint4 v[kHalf];
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k) {
+          const int idx = st + (round * kHalf + k) * 256;
+          const int r = idx / (HK / 8), c = idx % (HK / 8);
+          v[k] = make_uint4(0, 0, 0, 0);
+          if (round * kHalf + k < kPer && idx < kChunks && r < it.nrows) {
+            const int rr = it.r0 + r;
+            v[k] = *reinterpret_cast<const uint4*>(
+                P.query + (int64_t(it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G) * HK + c * 8);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k) {
+          const int idx = st + (round * kHalf + k) * 256;
+          const int r = idx / (HK / 8), c = idx % (HK / 8);
+          if (round * kHalf + k < kPer && idx < kChunks)
+            *reinterpret_cast<uint4*>(q_s + (c >> 3) * (kTcRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v[k];
+        }
+      }
+      fence_proxy_async();  // written by threads, read by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+    }
     const int quarter = warp & 3;             // TMEM lane quarter of this warp
     const int rh = (warp - 2) >> 2;           // which 32 of the 64 rows
     const bool active = lane < 16;            // M=64: lanes 0-15 of a quarter hold tokens
@@ -542,12 +554,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       } else {
 #pragma unroll
         for (int r = 0; r < 32; ++r) s[r] *= P.scale_log2;
-        if (P.mask_type == PA_MASK_NORM_COMPRESS && tok_ok && j > prefix) {
+        // the mask is read only above the diagonal (j > p): on and below it
+        // the pages fix it at 0; rows grow in position, so a token at or
+        // before this warp's first row position needs no read at all
+        if (P.mask_type == PA_MASK_NORM_COMPRESS && tok_ok && j > prefix + (it.r0 + rbase) / G) {
           const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
 #pragma unroll
           for (int r = 0; r < 32; ++r) {
-            const int mr = min(max(prow[rbase + r] - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
-            s[r] += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
+            const int pr = prow[rbase + r];
+            if (j > pr) {
+              const int mr = min(max(pr - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
+              s[r] += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
+            }
           }
         } else if (P.mask_type == PA_MASK_NORM && tok_ok) {
 #pragma unroll
