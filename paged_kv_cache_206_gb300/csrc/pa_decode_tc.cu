@@ -1,24 +1,21 @@
-// Instantiations and launcher of the tcgen05 decode kernel (64-row tiles).
+// Launcher of the tcgen05 decode kernel, and its 64-row instantiations.
 #include "pa_decode_tc.cuh"
 #include "pa_launch.h"
 
 namespace pa {
 
+template <>
+cudaError_t launch_tc_rows<64>(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdParams& P,
+                               int64_t n_items, cudaStream_t stream) {
+  return launch_tc_rows_impl<64>(tmk, tmv, P, n_items, stream, ensure_smem_attr);
+}
+
 cudaError_t launch_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdParams& P,
                       int64_t n_items, cudaStream_t stream) {
-  const TcLayout lay = tc_layout(P.hk);
-  auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), int(lay.bytes));
-    if (e != cudaSuccess) return e;
-    kern<<<unsigned(n_items), kTcThreads, lay.bytes, stream>>>(tmk, tmv, P);
-    return cudaGetLastError();
-  };
-  switch (P.hk * 1000 + P.hv) {
-    case 128128: return go(tc_decode_kernel<128, 128>);
-    case 256256: return go(tc_decode_kernel<256, 256>);
-    case 512512: return go(tc_decode_kernel<512, 512>);
-    case 576512: return go(tc_decode_kernel<576, 512>);
-    default: return cudaErrorInvalidValue;
+  switch (tc_tile_rows(P.group, P.mask_q)) {
+    case 16: return launch_tc_rows<16>(tmk, tmv, P, n_items, stream);
+    case 32: return launch_tc_rows<32>(tmk, tmv, P, n_items, stream);
+    default: return launch_tc_rows<64>(tmk, tmv, P, n_items, stream);
   }
 }
 

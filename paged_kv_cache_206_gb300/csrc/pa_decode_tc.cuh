@@ -60,33 +60,45 @@
 
 namespace pa {
 
-constexpr int kTcRows = PA_TC_TILE_ROWS;  // N of both MMAs (query rows, padded)
+constexpr int kTcRows = PA_TC_TILE_ROWS;  // rows of a tile at most; N of the PV MMA
 constexpr int kTcTok = 64;                // tokens per tile (M of QK^T)
-constexpr int kTcKSlots = 4;              // K ring of 16 KB boxes
-constexpr int kTcVSlots = 4;              // V ring of 16 KB boxes
 constexpr int kTcPBufs = 1;               // P^T buffers (softmax of tile n + kTcPBufs
                                           // waits for the PV of tile n)
+constexpr uint32_t kTcMaxSmem = 232448;   // dynamic shared memory a CTA may use
 constexpr uint32_t kTcHalfBytes = kTcTok * 128;      // 64 tokens x 64 dims x 2 B
 constexpr uint32_t kTcSlotBytes = 2 * kTcHalfBytes;  // 64 tokens x 128 dims
 constexpr int kTcThreads = 384;  // 2 producers, 2 MMA issuers, 8 softmax warps
 constexpr float kTcRescaleThreshold = 8.f;  // log2 units
 
-struct TcLayout {
-  uint32_t q_off, p_off, ring_off, red_off, rows_off, bars_off, tmem_slot_off, bytes;
+// Shared-memory plan of a launch with NR query rows per tile (16, 32 or 64:
+// the group's rows G * max_q rounded up): the query tile [hk/64][NR][128 B],
+// P^T [64 tokens][64 rows] (rows past NR stay zero), the K ring, the V ring,
+// the row exchange and constants, the barriers. The rings take what the query
+// tile leaves, at most 12 slots of 16 KB, split between K and V (K gets the
+// odd one: a sweep over ring sizes found K the more sensitive). With a
+// shared-KV cache (SH) there is no V ring: the PV MMAs read V from the K
+// slots, which then stay until the tile's PV is done, and every slot is K's.
+template <int HK, int NR, bool SH = false>
+struct TcCfg {
+  static constexpr uint32_t kQBytes = uint32_t(HK / 64) * NR * 128;
+  static constexpr uint32_t kOther = kTcPBufs * kTcTok * 128 + 4 * kTcRows * 4 +
+                                     6 * kTcRows * 4 + 12 * 8 + 16 + 1024;
+  static constexpr int kFit = int((kTcMaxSmem - kQBytes - kOther) / (kTcSlotBytes + 16));
+  static constexpr int kSlots = kFit < 12 ? kFit : 12;
+  static constexpr int kKSlots = SH ? kSlots : (kSlots + 1) / 2;
+  static constexpr int kVSlots = SH ? 0 : kSlots / 2;
+  static constexpr uint32_t q_off = 0;
+  static constexpr uint32_t p_off = q_off + kQBytes;
+  static constexpr uint32_t ring_off = p_off + kTcPBufs * kTcTok * 128;  // 1024-aligned
+  static constexpr uint32_t red_off = ring_off + kSlots * kTcSlotBytes;  // [4][64] fp32
+  static constexpr uint32_t rows_off = red_off + 4 * kTcRows * 4;        // per-row constants
+  static constexpr uint32_t bars_off = rows_off + 6 * kTcRows * 4;       // mbarriers
+  static constexpr uint32_t tmem_slot_off = bars_off + (2 * kSlots + 12) * 8;
+  static constexpr uint32_t bytes = tmem_slot_off + 16 + 1024;
+  static_assert(kKSlots >= 4 && (SH || kVSlots >= 4), "rings of at least one tile");
+  static_assert(!SH || kKSlots >= (HK / 64 + 1) / 2, "a shared-KV ring holds a whole tile");
+  static_assert(bytes <= kTcMaxSmem, "shared memory");
 };
-
-__host__ __device__ inline TcLayout tc_layout(int hk) {
-  TcLayout L;
-  L.q_off = 0;                                            // [hk/64][64 rows][128 B]
-  L.p_off = L.q_off + uint32_t(hk / 64) * kTcRows * 128;  // kTcPBufs x [64 tok][64 rows] fp16
-  L.ring_off = L.p_off + kTcPBufs * kTcTok * 128;         // K ring, then V ring
-  L.red_off = L.ring_off + (kTcKSlots + kTcVSlots) * kTcSlotBytes;  // [4][64] fp32 exchange
-  L.rows_off = L.red_off + 4 * kTcRows * 4;               // per-row constants
-  L.bars_off = L.rows_off + 6 * kTcRows * 4;              // mbarriers
-  L.tmem_slot_off = L.bars_off + (2 * (kTcKSlots + kTcVSlots) + 12) * 8;
-  L.bytes = L.tmem_slot_off + 16 + 1024;
-  return L;
-}
 
 // Head-size pairs the tcgen05 kernel is instantiated for (K and V move in
 // 16 KB slots of 64 tokens x 128 dims; a 576-dim K row takes four and a half).
@@ -170,6 +182,56 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
+// RH (8, 16 or 32) consecutive columns of this warp's TMEM lane quarter.
+template <int RH>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v) {
+  if constexpr (RH == 32) {
+    tmem_ld32(taddr, v);
+  } else if constexpr (RH == 16) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+          "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]),
+          "=f"(v[13]), "=f"(v[14]), "=f"(v[15])
+        : "r"(taddr)
+        : "memory");
+  } else {
+    static_assert(RH == 8, "8, 16 or 32 columns");
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                   "=f"(v[6]), "=f"(v[7])
+                 : "r"(taddr)
+                 : "memory");
+  }
+}
+
+template <int RH>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float* v) {
+  if constexpr (RH == 32) {
+    tmem_st32(taddr, *reinterpret_cast<const float(*)[32]>(v));
+  } else if constexpr (RH == 16) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+  } else {
+    static_assert(RH == 8, "8, 16 or 32 columns");
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+        : "memory");
+  }
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -209,24 +271,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int la
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// Butterfly reduce-scatter (sum) of v[32] across the warp: afterwards lane l
-// holds, in v[0], the sum over the 32 lanes of element l.
-__device__ __forceinline__ void reduce_scatter32_add(float (&v)[32], int lane) {
+// Sum over the warp.
+__device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
-  for (int lvl = 0; lvl < 5; ++lvl) {
-    const int off = 16 >> lvl;
-    const int half = 16 >> lvl;  // values kept after this level
-    const bool upper = lane & off;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-    }
-  }
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
 }
 
-template <int HK, int HV>
+template <int HK, int HV, int NR, bool SH>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
     const FwdParams P) {
@@ -235,35 +287,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
                                       // last holds one half when KH is odd)
   constexpr int VS = HV / 128;  // V slots per tile = O^T chunks of 128 dims
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kIdescQK = mma_idesc(64, kTcRows, 0, 0);
+  using Cfg = TcCfg<HK, NR, SH>;
+  constexpr int kKSlots = Cfg::kKSlots, kVSlots = Cfg::kVSlots;
+  constexpr int RH = NR / 2;  // rows per softmax thread (two warps per lane quarter)
+  constexpr uint32_t kIdescQK = mma_idesc(64, NR, 0, 0);
   constexpr uint32_t kIdescPV = mma_idesc(128, kTcRows, 1, 1);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
-  const TcLayout lay = tc_layout(HK);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint8_t* q_s = smem + lay.q_off;
-  uint8_t* p_s = smem + lay.p_off;
-  uint8_t* kring = smem + lay.ring_off;
-  uint8_t* vring = kring + kTcKSlots * kTcSlotBytes;
-  float* red = reinterpret_cast<float*>(smem + lay.red_off);
-  float* m_used = reinterpret_cast<float*>(smem + lay.rows_off);  // [64] reference max (base 2)
+  uint8_t* q_s = smem + Cfg::q_off;
+  uint8_t* p_s = smem + Cfg::p_off;
+  uint8_t* kring = smem + Cfg::ring_off;
+  uint8_t* vring = kring + kKSlots * kTcSlotBytes;
+  float* red = reinterpret_cast<float*>(smem + Cfg::red_off);
+  float* m_used = reinterpret_cast<float*>(smem + Cfg::rows_off);  // [64] reference max (base 2)
   float* alpha_s = m_used + kTcRows;                              // [64] rescale factors
   float* slope2 = alpha_s + kTcRows;                              // [64]
   int* prow = reinterpret_cast<int*>(slope2 + kTcRows);           // [64]
   float* l_tot = slope2 + 2 * kTcRows;                            // [64]
   int* flags = reinterpret_cast<int*>(l_tot + kTcRows);           // [1] rescale this tile
-  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + lay.bars_off);
-  uint64_t* kempty = kfull + kTcKSlots;
-  uint64_t* vfull = kempty + kTcKSlots;
-  uint64_t* vempty = vfull + kTcVSlots;
-  uint64_t* s_full = vempty + kTcVSlots;  // [2] S^T buffer ready
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Cfg::bars_off);
+  uint64_t* kempty = kfull + kKSlots;
+  uint64_t* vfull = kempty + kKSlots;
+  uint64_t* vempty = vfull + kVSlots;
+  uint64_t* s_full = vempty + kVSlots;  // [2] S^T buffer ready
   uint64_t* s_free = s_full + 2;          // [2] S^T buffer read by every softmax warp
   uint64_t* p_full = s_full + 4;          // [2] P^T buffer written
   uint64_t* pv_done = s_full + 6;         // [2] PV that read P^T buffer b complete
   uint64_t* qk_done = s_full + 8;         // every QK MMA complete
   uint64_t* o_done = s_full + 9;          // every PV MMA complete
   uint64_t* q_ready = s_full + 10;        // query tile in shared memory (one arrival per softmax warp)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.tmem_slot_off);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::tmem_slot_off);
 
   if (P.counts && int(blockIdx.x) >= P.counts[0]) return;  // past a device plan's items
   Item it;
@@ -285,11 +339,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
 
   // ---- set-up: barriers, TMEM, query tile, per-row constants
   if (tid == 0) {
-    for (int s = 0; s < kTcKSlots; ++s) {
+    for (int s = 0; s < kKSlots; ++s) {
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
     }
-    for (int s = 0; s < kTcVSlots; ++s) {
+    for (int s = 0; s < kVSlots; ++s) {
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 1);
     }
@@ -328,9 +382,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
 
   if (warp == 0 || warp == 10) {
     // ================= TMA producers (lane 0): K (warp 0), V (warp 10) =========
-    if (lane == 0) {
+    if (lane == 0 && !(SH && warp == 10)) {
       const bool is_k = warp == 0;
-      const int nslots = is_k ? kTcKSlots : kTcVSlots;
+      const int nslots = is_k ? kKSlots : kVSlots;
       uint8_t* ring = is_k ? kring : vring;
       uint64_t* full = is_k ? kfull : vfull;
       uint64_t* empty = is_k ? kempty : vempty;
@@ -416,8 +470,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       if (m >= 2 && !warp_wait(&s_free[m & 1], ((m >> 1) - 1) & 1, lane)) { ok = false; break; }
       tc_fence_after();
       for (int ks = 0; ks < KS; ++ks, ++consumed) {
-        const int slot = consumed % kTcKSlots;
-        if (!warp_wait(&kfull[slot], (consumed / kTcKSlots) & 1, lane)) { ok = false; break; }
+        const int slot = consumed % kKSlots;
+        if (!warp_wait(&kfull[slot], (consumed / kKSlots) & 1, lane)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
@@ -426,11 +480,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint64_t a = smem_desc(ring_addr + slot * kTcSlotBytes + h * kTcHalfBytes + k * 32, 16, 1024);
-              const uint64_t b = smem_desc(q_addr + (2 * ks + h) * (kTcRows * 128) + k * 32, 16, 1024);
+              const uint64_t b = smem_desc(q_addr + (2 * ks + h) * (NR * 128) + k * 32, 16, 1024);
               tc_mma(tmem_s + (m & 1) * 64, a, b, kIdescQK, (ks | h | k) != 0);
             }
           }
-          tc_commit(&kempty[slot]);
+          if (!SH) tc_commit(&kempty[slot]);  // shared KV: released after the PV
         }
         __syncwarp();
       }
@@ -444,7 +498,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   } else if (warp == 11) {
     // ================= PV issuer =================
     bool ok = true;
-    const uint32_t p_addr = smem_u32(p_s), ring_addr = smem_u32(vring);
+    uint8_t* const ring = SH ? kring : vring;  // shared KV: V is in the K slots
+    const uint32_t p_addr = smem_u32(p_s), ring_addr = smem_u32(ring);
     int consumed = 0;
     for (int n = 0; n < ntiles && ok; ++n) {
       const int pb = n % kTcPBufs;
@@ -452,15 +507,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       tc_fence_after();
       const int nvalid = min(kTcTok, it.tok1 - (it.tok0 + n * kTcTok));
       for (int oc = 0; oc < VS; ++oc, ++consumed) {
-        const int slot = consumed % kTcVSlots;
-        if (!warp_wait(&vfull[slot], (consumed / kTcVSlots) & 1, lane)) { ok = false; break; }
+        // shared KV: chunk oc is K slot oc of tile n (already waited on by the
+        // QK issuer; this wait returns at once and orders the reads after the copy)
+        const int ring_slots = SH ? kKSlots : kVSlots;
+        const int seq = SH ? n * KS + oc : consumed;
+        const int slot = seq % ring_slots;
+        if (!warp_wait(SH ? &kfull[slot] : &vfull[slot], (seq / ring_slots) & 1, lane)) { ok = false; break; }
         if (nvalid < kTcTok) {
           // V rows of tokens past the range may hold anything (NaN included):
           // zero them (both 64-dim halves) so that p = 0 contributes nothing.
           const int per = (kTcTok - nvalid) * 8;
           for (int idx = lane; idx < 2 * per; idx += 32) {
             const int h = idx / per, rem = idx % per;
-            *reinterpret_cast<uint4*>(vring + slot * kTcSlotBytes + h * kTcHalfBytes +
+            *reinterpret_cast<uint4*>(ring + slot * kTcSlotBytes + h * kTcHalfBytes +
                                       (nvalid + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async();
@@ -474,11 +533,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
             const uint64_t b = smem_desc(p_addr + pb * (kTcTok * 128) + k * 2048, kTcHalfBytes, 1024);
             tc_mma(tmem_o + oc * 64, a, b, kIdescPV, (n | k) != 0);
           }
-          tc_commit(&vempty[slot]);
+          if (!SH) tc_commit(&vempty[slot]);
         }
         __syncwarp();
       }
       if (!ok) break;
+      if (SH && lane == 0)  // every K slot of tile n (the last one too) is free once its PV is done
+        for (int sl = 0; sl < KS; ++sl) tc_commit(&kempty[(n * KS + sl) % kKSlots]);
       if (lane == 0) tc_commit(&pv_done[pb]);
       __syncwarp();
     }
@@ -492,7 +553,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     // rounds whose loads are all issued before their stores.
     {
       const int st = tid - 64;  // 0..255
-      constexpr int kChunks = kTcRows * (HK / 8);
+      constexpr int kChunks = NR * (HK / 8);
       constexpr int kPer = (kChunks + 255) / 256;
       constexpr int kHalf = (kPer + 1) / 2;
 #pragma unroll
@@ -514,9 +575,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
           const int idx = st + (round * kHalf + k) * 256;
           const int r = idx / (HK / 8), c = idx % (HK / 8);
           if (round * kHalf + k < kPer && idx < kChunks)
-            *reinterpret_cast<uint4*>(q_s + (c >> 3) * (kTcRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v[k];
+            *reinterpret_cast<uint4*>(q_s + (c >> 3) * (NR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v[k];
         }
       }
+      if (NR < kTcRows)  // P^T columns past NR are read by the PV MMA: keep them zero
+        for (int i = st; i < kTcPBufs * kTcTok * 8; i += 256)
+          reinterpret_cast<uint4*>(p_s)[i] = make_uint4(0, 0, 0, 0);
       fence_proxy_async();  // written by threads, read by the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
@@ -526,20 +590,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const bool active = lane < 16;            // M=64: lanes 0-15 of a quarter hold tokens
     const int tt = quarter * 16 + lane;       // token within the tile (active lanes)
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    const int rbase = rh * 32;
+    const int rbase = rh * RH;
     // This token's probabilities summed over the tiles, for rows rbase + r,
     // relative to the row's reference max; reduced across tokens at the end.
-    float l_t[32];
+    float l_t[RH];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) l_t[r] = 0.f;
+    for (int r = 0; r < RH; ++r) l_t[r] = 0.f;
     const float4* m_used4 = reinterpret_cast<const float4*>(m_used + rbase);
     bool ok = true;
     for (int n = 0; n < ntiles; ++n) {
       const bool got = mbar_wait(&s_full[n & 1], (n >> 1) & 1);
       if (softmax_bar_or(!got)) { ok = false; break; }  // all softmax warps agree
       tc_fence_after();
-      float s[32];
-      tmem_ld32(tmem_s + (n & 1) * 64 + lane_base + rbase, s);
+      float s[RH];
+      tmem_ld<RH>(tmem_s + (n & 1) * 64 + lane_base + rbase, s);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -549,18 +613,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       // scores in base 2, plus bias; tokens past the range drop out
       if (P.mask_type == PA_MASK_ALIBI) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
+        for (int r = 0; r < RH; ++r)
           s[r] = s[r] * P.scale_log2 + slope2[rbase + r] * float(j - prow[rbase + r]);
       } else {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) s[r] *= P.scale_log2;
+        for (int r = 0; r < RH; ++r) s[r] *= P.scale_log2;
         // the mask is read only above the diagonal (j > p): on and below it
         // the pages fix it at 0; rows grow in position, so a token at or
         // before this warp's first row position needs no read at all
         if (P.mask_type == PA_MASK_NORM_COMPRESS && tok_ok && j > prefix + (it.r0 + rbase) / G) {
           const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
 #pragma unroll
-          for (int r = 0; r < 32; ++r) {
+          for (int r = 0; r < RH; ++r) {
             const int pr = prow[rbase + r];
             if (j > pr) {
               const int mr = min(max(pr - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
@@ -569,18 +633,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
           }
         } else if (P.mask_type == PA_MASK_NORM && tok_ok) {
 #pragma unroll
-          for (int r = 0; r < 32; ++r) s[r] += norm_mask_log2(P, it.b, prow[rbase + r] - prefix, j);
+          for (int r = 0; r < RH; ++r) s[r] += norm_mask_log2(P, it.b, prow[rbase + r] - prefix, j);
         }
       }
       if (!tok_ok) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) s[r] = -INFINITY;
+        for (int r = 0; r < RH; ++r) s[r] = -INFINITY;
       }
       // Is any score above its row's reference max by more than the threshold?
       // (Always on the first tile, where the references are -inf.)
       float ex = -INFINITY;
 #pragma unroll
-      for (int r4 = 0; r4 < 8; ++r4) {
+      for (int r4 = 0; r4 < RH / 4; ++r4) {
         const float4 m = m_used4[r4];
         ex = fmaxf(ex, fmaxf(fmaxf(s[4 * r4] - m.x, s[4 * r4 + 1] - m.y),
                              fmaxf(s[4 * r4 + 2] - m.z, s[4 * r4 + 3] - m.w)));
@@ -590,17 +654,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         // exact tile max per row: warp max, then across the 4 lane quarters
         float keep = 0.f;
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
+        for (int r = 0; r < RH; ++r) {
           const float wm = warp_max(s[r]);
           if (r == lane) keep = wm;
         }
-        red[quarter * 64 + rbase + lane] = keep;
+        if (lane < RH) red[quarter * 64 + rbase + lane] = keep;
         softmax_bar();
         if (warp == 2) {
           bool grow = false;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int r = lane + 32 * e;
+            if (r >= NR) break;
             const float mt = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
             const float mu = m_used[r];
             const float nm = fmaxf(mt, mu);
@@ -615,12 +680,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         grew = flags[1] != 0;
         if (grew) {
 #pragma unroll
-          for (int r = 0; r < 32; ++r) l_t[r] *= alpha_s[rbase + r];
+          for (int r = 0; r < RH; ++r) l_t[r] *= alpha_s[rbase + r];
         }
       }
       // probabilities and per-token sums
 #pragma unroll
-      for (int r4 = 0; r4 < 8; ++r4) {
+      for (int r4 = 0; r4 < RH / 4; ++r4) {
         const float4 m = m_used4[r4];
         s[4 * r4] = ex2(s[4 * r4] - m.x);
         s[4 * r4 + 1] = ex2(s[4 * r4 + 1] - m.y);
@@ -628,7 +693,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         s[4 * r4 + 3] = ex2(s[4 * r4 + 3] - m.w);
       }
 #pragma unroll
-      for (int r = 0; r < 32; ++r) l_t[r] += s[r];
+      for (int r = 0; r < RH; ++r) l_t[r] += s[r];
       // P^T buffer n % kTcPBufs was last read by PV(n - kTcPBufs); a rescale
       // of O^T also needs PV(n - 1). Each wait is on the barrier of that PV's
       // P^T buffer, whose next phase needs P^T(n) and so cannot have begun.
@@ -645,13 +710,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       // 4 rh .. 4 rh + 3 of the 128-byte row
       if (active) {
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
+        for (int c8 = 0; c8 < RH / 8; ++c8) {
           uint4 pk;
           pk.x = pack_half2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
           pk.y = pack_half2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
           pk.z = pack_half2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
           pk.w = pack_half2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
-          const int chunk = 4 * rh + c8;
+          const int chunk = rh * (RH / 8) + c8;
           *reinterpret_cast<uint4*>(p_s + (n % kTcPBufs) * (kTcTok * 128) + tt * 128 + ((chunk ^ (tt & 7)) << 4)) = pk;
         }
       }
@@ -660,13 +725,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         // its 32 rows, before this tile's PV (PV of the previous tile is done).
 #pragma unroll 1
         for (int oc = 0; oc < VS; ++oc) {
-          float o[32];
+          float o[RH];
           const uint32_t ta = tmem_o + oc * 64 + rbase + lane_base;
-          tmem_ld32(ta, o);
+          tmem_ld<RH>(ta, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha_s[rbase + i];
-          tmem_st32(ta, o);
+          for (int i = 0; i < RH; ++i) o[i] *= alpha_s[rbase + i];
+          tmem_st<RH>(ta, o);
         }
         tmem_wait_st();
       }
@@ -678,13 +743,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const int t = quarter * 32 + lane;  // TMEM lane of this thread = output dim in a chunk
     if (!ok && t == 0 && rh == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
     // ---- epilogue: row sums across all tokens, then O^T / l
-    reduce_scatter32_add(l_t, lane);  // lane l: rows rbase + l, this warp's tokens
-    red[quarter * 64 + rbase + lane] = l_t[0];
+    {
+      float mine = 0.f;  // lane l < RH: row rbase + l, summed over this warp's tokens
+#pragma unroll
+      for (int r = 0; r < RH; ++r) {
+        const float t = warp_sum(l_t[r]);
+        if (r == lane) mine = t;
+      }
+      if (lane < RH) red[quarter * 64 + rbase + lane] = mine;
+    }
     softmax_bar();
     if (warp == 2) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int r = lane + 32 * e;
+        if (r >= NR) break;
         l_tot[r] = (red[r] + red[64 + r]) + (red[128 + r] + red[192 + r]);
       }
     }
@@ -699,12 +772,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
 #pragma unroll 1
       for (int oc = 0; oc < VS; ++oc) {
         const int d = oc * 128 + t;  // output dim of this thread
-        float o[32];
-        tmem_ld32(tmem_o + oc * 64 + rbase + lane_base, o);
+        float o[RH];
+        tmem_ld<RH>(tmem_o + oc * 64 + rbase + lane_base, o);
         tmem_wait_ld();
         if (!fits) continue;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < RH; ++i) {
           const int r = rbase + i;
           if (r >= it.nrows) break;
           const float val = o[i] / l_tot[r];
@@ -741,7 +814,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   }
 }
 
+// Launch with NR rows per tile (instantiated in pa_decode_tc.cu, _n16.cu, _n32.cu).
+template <int NR>
+cudaError_t launch_tc_rows(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdParams& P,
+                           int64_t n_items, cudaStream_t stream);
+
+// Rows per tile of a launch: the group's rows G * max_q rounded up to 16, 32 or 64.
+inline int tc_tile_rows(int group, int max_q) {
+  const int r = group * max_q;
+  return r <= 16 ? 16 : (r <= 32 ? 32 : 64);
+}
+
 cudaError_t launch_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdParams& P,
                       int64_t n_items, cudaStream_t stream);
+
+// One launcher body for every NR: the head-size pairs of tc_supported.
+template <int NR>
+cudaError_t launch_tc_rows_impl(const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                const FwdParams& P, int64_t n_items, cudaStream_t stream,
+                                cudaError_t (*set_attr)(const void*, int)) {
+  auto go = [&](auto kern, uint32_t bytes) -> cudaError_t {
+    cudaError_t e = set_attr(reinterpret_cast<const void*>(kern), int(bytes));
+    if (e != cudaSuccess) return e;
+    kern<<<unsigned(n_items), kTcThreads, bytes, stream>>>(tmk, tmv, P);
+    return cudaGetLastError();
+  };
+  const bool sh = P.kv_shared != 0;
+  switch (P.hk * 1000 + P.hv) {
+    case 128128:
+      return sh ? go(tc_decode_kernel<128, 128, NR, true>, TcCfg<128, NR, true>::bytes)
+                : go(tc_decode_kernel<128, 128, NR, false>, TcCfg<128, NR>::bytes);
+    case 256256:
+      return sh ? go(tc_decode_kernel<256, 256, NR, true>, TcCfg<256, NR, true>::bytes)
+                : go(tc_decode_kernel<256, 256, NR, false>, TcCfg<256, NR>::bytes);
+    case 512512:
+      return sh ? go(tc_decode_kernel<512, 512, NR, true>, TcCfg<512, NR, true>::bytes)
+                : go(tc_decode_kernel<512, 512, NR, false>, TcCfg<512, NR>::bytes);
+    case 576512:
+      return sh ? go(tc_decode_kernel<576, 512, NR, true>, TcCfg<576, NR, true>::bytes)
+                : go(tc_decode_kernel<576, 512, NR, false>, TcCfg<576, NR>::bytes);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 }  // namespace pa
