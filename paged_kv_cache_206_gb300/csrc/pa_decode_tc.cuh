@@ -753,12 +753,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       if (lane < RH) red[quarter * 64 + rbase + lane] = mine;
     }
     softmax_bar();
+    const bool partial = it.slot >= 0;
+    const bool fits = !partial || int64_t(it.slot) + it.nrows <= P.part_rows_cap;
+    // Per-row work of the epilogue, once (warp 2): the row's 1/l, its LSE (split
+    // items) and its output row (whole items). The arrays reused here are no
+    // longer read by the softmax loop. Keeping this out of the per-element loop
+    // keeps that loop small; a per-element version spent ~20 us per item.
+    float* inv_l = alpha_s;
+    int* out_row = prow;
     if (warp == 2) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int r = lane + 32 * e;
         if (r >= NR) break;
-        l_tot[r] = (red[r] + red[64 + r]) + (red[128 + r] + red[192 + r]);
+        const float l = (red[r] + red[64 + r]) + (red[128 + r] + red[192 + r]);
+        l_tot[r] = l;
+        inv_l[r] = 1.f / l;
+        const int rr = it.r0 + r;
+        out_row[r] = (it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G;
+        if (partial && fits && r < it.nrows && ntiles > 0)
+          P.part_lse[it.slot + r] = (m_used[r] + log2f(l)) * kLn2;
       }
     }
     launch_dependents();
@@ -766,8 +780,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const bool done = !softmax_bar_or(!got);
     if (done && ntiles > 0) {
       tc_fence_after();
-      const bool partial = it.slot >= 0;
-      const bool fits = !partial || int64_t(it.slot) + it.nrows <= P.part_rows_cap;
       if (!fits && t == 0 && rh == 0) set_status(P.status, PA_STATUS_BIT_WORKSPACE);
 #pragma unroll 1
       for (int oc = 0; oc < VS; ++oc) {
@@ -776,19 +788,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         tmem_ld<RH>(tmem_o + oc * 64 + rbase + lane_base, o);
         tmem_wait_ld();
         if (!fits) continue;
+        if (partial) {
+          float* dst = P.part_o + (int64_t(it.slot) + rbase) * HV + d;
 #pragma unroll
-        for (int i = 0; i < RH; ++i) {
-          const int r = rbase + i;
-          if (r >= it.nrows) break;
-          const float val = o[i] / l_tot[r];
-          if (!partial) {
-            const int rr = it.r0 + r;
-            P.out[(int64_t(it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G) * HV + d] =
-                __float2half_rn(val);
-          } else {
-            P.part_o[(int64_t(it.slot) + r) * HV + d] = val;
-            if (d == 0) P.part_lse[it.slot + r] = (m_used[r] + log2f(l_tot[r])) * kLn2;
-          }
+          for (int i = 0; i < RH; ++i)
+            if (rbase + i < it.nrows) dst[int64_t(i) * HV] = o[i] * inv_l[rbase + i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < RH; ++i)
+            if (rbase + i < it.nrows)
+              P.out[int64_t(out_row[rbase + i]) * HV + d] = __float2half_rn(o[i] * inv_l[rbase + i]);
         }
       }
     } else if (done && it.slot >= 0 && int64_t(it.slot) + it.nrows <= P.part_rows_cap) {
