@@ -146,13 +146,16 @@ typedef struct pa_config {
  * Chunk. NB_b = ceil(L_b / bs). With chunk_blocks > 0, c = chunk_blocks.
  * Otherwise
  *   W     = sum_b NB_b * Hk * QT_b
- *   c_bal = ceil(W / (8 * num_sms))
+ *   k     = 8 if TR <= PA_FMA_MAX_ROWS, else 2
+ *   c_bal = ceil(W / (k * num_sms))
  *   RT    = min(TR, G * max_seqlen_q)   (rows a full tile really holds)
  *   c_min = ceil(64 * RT * hv / (bs * (hk + hv)))
  *   c     = max(1, c_bal, c_min)
- * (c_bal aims at about eight work items per SM so that variable lengths
- * balance; c_min keeps the partial results that a split writes and re-reads
- * below about a sixteenth of the KV bytes of the split.)
+ * (c_bal aims at about k work items per SM so that variable lengths
+ * balance: eight for the CUDA-core and mma.sync kernels, of which several CTAs
+ * share an SM, two for the tcgen05 kernel, which holds an SM alone and pays a
+ * longer fixed cost per item; c_min keeps the partial results that a split
+ * writes and re-reads below about a sixteenth of the KV bytes of the split.)
  * Sequence b has S_b = ceil(NB_b / c) splits; split s covers KV blocks
  * [s * c, min(NB_b, (s + 1) * c)).
  *

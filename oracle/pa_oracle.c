@@ -197,9 +197,10 @@ static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
  *   tiles          QT_b = ceil(G * q_b / TR)
  *   blocks         NB_b = ceil(L_b / bs)
  *   chunk          c = chunk_blocks if positive, else
- *                  max(1, ceil(sum_b NB_b*Hk*QT_b / (8*num_sms)),
+ *                  max(1, ceil(sum_b NB_b*Hk*QT_b / (k*num_sms)),
  *                         ceil(64*RT*hv / (bs*(hk+hv))))
- *                  with RT = min(TR, G * maxq), the rows a full tile holds
+ *                  with RT = min(TR, G * maxq), the rows a full tile holds,
+ *                  and k = 8 when TR <= 8, else 2
  *   splits         S_b = ceil(NB_b / c); split s = blocks [s*c, min(NB_b, (s+1)*c))
  *   items          (b, kvh, qt, s) lexicographic; 8 ints
  *                  {b, kvh, row_begin, row_end, kb_begin, kb_end, q_start, slot}
@@ -224,7 +225,8 @@ int oracle_plan(int batch, int num_heads, int kv_heads, int hk, int hv, int bloc
       const int64_t q = q_seqlens ? q_seqlens[b] : 1;
       W += cdiv(context_lens[b], block_size) * kv_heads * cdiv(G * q, TR);
     }
-    const int64_t c_bal = cdiv(W, 8 * (int64_t)num_sms);
+    const int64_t per_sm = TR <= 8 ? 8 : 2;
+    const int64_t c_bal = cdiv(W, per_sm * (int64_t)num_sms);
     const int64_t RT = TR < G * maxq ? TR : G * maxq;
     const int64_t c_min = cdiv(64 * RT * hv, (int64_t)block_size * (hk + hv));
     c = 1;

@@ -3,7 +3,8 @@
 // restated for one GPU. Each split s of a query tile left a normalised partial
 // output O_s and its log-sum-exp lse_s; the merged row is
 //   out = sum_s exp(lse_s - M) * O_s / sum_s exp(lse_s - M),  M = max_s lse_s.
-// One warp merges one row; a CTA takes kCombineRows rows of one combine entry.
+// One warp merges 128 dims of one row; a CTA takes eight rows of one combine
+// entry and one 128-dim slice (grid z).
 #include "pa_combine.cuh"
 #include "pa_device.cuh"
 
@@ -43,11 +44,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   const int r = r0 + rr, i = r / C.group, h = kvh * C.group + r % C.group;
   __half* dst = C.out + (int64_t(q_start + i) * C.num_heads + h) * C.hv;
   const float* po = C.part_o + (int64_t(slot0) + rr) * C.hv;
-  for (int d = lane * 4; d < C.hv; d += 128) {
+  const int64_t split_stride = int64_t(nrows) * C.hv;
+  // this warp's 128 dims (blockIdx.z); loads of several splits in flight at once
+  const int d = blockIdx.z * 128 + lane * 4;
+  if (d < C.hv) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (int s = 0; s < S; ++s) {
       const float w = s < kCombineMaxSplits ? wts[warp][s] : __expf(lse[int64_t(s) * nrows] - M);
-      const float4 v = *reinterpret_cast<const float4*>(po + int64_t(s) * nrows * C.hv + d);
+      const float4 v = __ldg(reinterpret_cast<const float4*>(po + s * split_stride + d));
       acc.x += w * v.x;
       acc.y += w * v.y;
       acc.z += w * v.z;
@@ -66,7 +71,8 @@ cudaError_t launch_combine(const CombineParams& C, int64_t n_combine, int tile_r
                            cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(n_combine),
-                     unsigned((tile_rows + kCombineThreads / 32 - 1) / (kCombineThreads / 32)));
+                     unsigned((tile_rows + kCombineThreads / 32 - 1) / (kCombineThreads / 32)),
+                     unsigned((C.hv + 127) / 128));
   cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

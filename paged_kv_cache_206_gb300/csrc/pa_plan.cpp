@@ -86,7 +86,10 @@ extern "C" pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens,
   if (c.chunk_blocks > 0) {
     chunk = c.chunk_blocks;
   } else {
-    const int64_t bal = cdiv(W, 8 * int64_t(c.num_sms));
+    // items per SM aimed at: 8 for the warp kernels (several CTAs per SM), 2
+    // for the tcgen05 kernel (one CTA per SM, a longer fixed cost per item)
+    const int64_t per_sm = TR <= PA_FMA_MAX_ROWS ? 8 : 2;
+    const int64_t bal = cdiv(W, per_sm * int64_t(c.num_sms));
     const int64_t RT = std::min(TR, G * maxq);  // rows a full tile really holds
     const int64_t lo = cdiv(64 * RT * c.head_size_v, bs * (c.head_size_k + c.head_size_v));
     chunk = std::max<int64_t>(1, std::max(bal, lo));

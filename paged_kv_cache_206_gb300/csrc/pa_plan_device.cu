@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanPara
   if (tid == 0) {
     int64_t c = D.chunk_blocks;
     if (c <= 0) {
-      c = dcdiv(W, 8 * int64_t(D.num_sms));
+      c = dcdiv(W, (TR <= PA_FMA_MAX_ROWS ? 8 : 2) * int64_t(D.num_sms));
       const int64_t RT = TR < int64_t(G) * D.maxq ? TR : int64_t(G) * D.maxq;  // real rows
       const int64_t lo = dcdiv(int64_t(64) * RT * D.hv, int64_t(bs) * (D.hk + D.hv));
       if (lo > c) c = lo;
