@@ -12,6 +12,7 @@
 #include "pa_combine.cuh"
 #include "pa_decode_mma.cuh"
 #include "pa_decode_tc.cuh"
+#include "pa_prefill_tc.cuh"
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_plan_device.h"
@@ -248,6 +249,17 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
       case 4: err = launch_fma<4>(tmk, tmv, P, n_items, stream); break;
       default: err = launch_fma<8>(tmk, tmv, P, n_items, stream); break;
     }
+  } else if (int64_t(P.group) * max_q(c) > PA_TC_TILE_ROWS && pf_supported(hk, hv)) {
+    // rows meet many keys (prefill, or more than one 64-row tile per kv head):
+    // 128-token key tiles, boxes of min(block_size, 128) tokens, both 64-dim
+    // halves in one box at 128
+    const int rows = c.block_size < 128 ? c.block_size : 128;
+    const int halves = rows == 128 ? hk / 64 : 1;
+    CUtensorMap tmk, tmv;
+    if (!cache_map_3d(&tmk, key_cache, c, hk, rows, halves) ||
+        !cache_map_3d(&tmv, value_cache, c, kv_shared ? hk : hv, rows, halves))
+      return PA_ERR_CUDA;
+    err = launch_pf(tmk, tmv, P, n_items, stream);
   } else {
     // 64-row tiles on the tcgen05 kernel: boxes of min(block_size, 64) tokens
     if (!tc_supported(hk, hv)) return PA_ERR_UNSUPPORTED;

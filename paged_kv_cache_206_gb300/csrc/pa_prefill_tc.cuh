@@ -1,0 +1,462 @@
+// Paged attention for tiles whose rows meet many keys (prefill, q = L, and any
+// launch whose group rows G * max_q exceed one 64-row tile), on the tcgen05
+// tensor cores. Same operation, work item and split/merge contract as the
+// decode kernels (PagedAttentionOperation semantics; task list and FlashDecode
+// merge of the SparseAttnSharedkvMetadata page); a different tile shape.
+//
+// One CTA per work item (64 query rows), 128-token key tiles, 8 warps:
+//   warp 0     TMA producer: K and V of each key tile (3-D boxes, 128-byte
+//              swizzle) into a 3-slot K ring and a 2-slot V ring.
+//   warp 1     allocates TMEM; one thread issues S = Q . K^T (M=64 rows,
+//              N=128 tokens, K-major operands; S double-buffered in TMEM),
+//              then O += P . V for the previous tile (M=64, N=hd; A = P
+//              K-major, B = V MN-major; O accumulates in TMEM).
+//   warps 4-7  softmax, one query row per thread (M=64 puts rows 16q..16q+15
+//              in lanes 0-15 of TMEM lane quarter q): the row's scores come
+//              from TMEM in 32-column loads, so max and sum need no exchange
+//              between threads. The reference max is moved (and O rescaled in
+//              TMEM) only when a score exceeds it by more than 2^8. P (fp16)
+//              goes to shared memory, double-buffered, in the K-major
+//              swizzled layout the PV MMA reads.
+//   warps 2-3  no role.
+// With the compressed causal mask an item stops after its last query row's
+// position, and only the keys above the diagonal read the mask. Every wait is
+// bounded; on a timeout the CTA records PA_STATUS_BIT_TIMEOUT and exits
+// cleanly.
+#pragma once
+
+#include "pa_decode_tc.cuh"
+
+namespace pa {
+
+constexpr int kPfTok = 128;      // key tokens per tile (N of S = Q . K^T)
+constexpr int kPfRows = 64;      // query rows per tile (M of both MMAs)
+constexpr int kPfThreads = 256;  // 8 warps
+constexpr int kPfKSlots = 3;
+constexpr int kPfVSlots = 2;
+constexpr int kPfPBufs = 2;
+
+template <int HD>
+struct PfCfg {
+  static constexpr int kHalves = HD / 64;                       // 64-dim halves of a row
+  static constexpr uint32_t kSlot = uint32_t(kPfTok) * HD * 2;  // one K or V tile
+  static constexpr uint32_t kQ = uint32_t(kPfRows) * HD * 2;
+  static constexpr uint32_t kP = uint32_t(kPfRows) * kPfTok * 2;
+  static constexpr uint32_t q_off = 0;
+  static constexpr uint32_t p_off = q_off + kQ;
+  static constexpr uint32_t k_off = p_off + kPfPBufs * kP;
+  static constexpr uint32_t v_off = k_off + kPfKSlots * kSlot;
+  static constexpr uint32_t bars_off = v_off + kPfVSlots * kSlot;
+  static constexpr int kBars = 2 * (kPfKSlots + kPfVSlots) + 12;
+  static constexpr uint32_t tmem_slot_off = bars_off + kBars * 8;
+  static constexpr uint32_t bytes = tmem_slot_off + 16 + 1024;
+  static_assert(bytes <= kTcMaxSmem, "shared memory");
+};
+
+inline bool pf_supported(int hk, int hv) { return hk == hv && (hk == 64 || hk == 128); }
+
+template <int HD>
+__global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
+    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+    const FwdParams P) {
+  using Cfg = PfCfg<HD>;
+  constexpr int H2 = Cfg::kHalves;
+  constexpr uint32_t kTmemCols = 512;
+  constexpr uint32_t kIdescQK = mma_idesc(kPfRows, kPfTok, 0, 0);
+  constexpr uint32_t kIdescPV = mma_idesc(kPfRows, HD, 0, 1);
+  constexpr uint32_t kHalfK = uint32_t(kPfTok) * 128;  // one 64-dim half of a K/V tile
+  constexpr uint32_t kHalfQ = uint32_t(kPfRows) * 128;  // one 64-dim half of Q
+  constexpr uint32_t kHalfP = uint32_t(kPfRows) * 128;  // one 64-token half of P
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = aligned_smem(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint8_t* q_s = smem + Cfg::q_off;
+  uint8_t* p_s = smem + Cfg::p_off;
+  uint8_t* kring = smem + Cfg::k_off;
+  uint8_t* vring = smem + Cfg::v_off;
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Cfg::bars_off);
+  uint64_t* kempty = kfull + kPfKSlots;
+  uint64_t* vfull = kempty + kPfKSlots;
+  uint64_t* vempty = vfull + kPfVSlots;
+  uint64_t* s_full = vempty + kPfVSlots;  // [2] S buffer written
+  uint64_t* s_free = s_full + 2;          // [2] S buffer read by the softmax warps
+  uint64_t* p_full = s_full + 4;          // [2] P buffer written
+  uint64_t* pv_done = s_full + 6;         // [2] PV that read P buffer b complete
+  uint64_t* qk_done = s_full + 8;
+  uint64_t* o_done = s_full + 9;
+  uint64_t* q_ready = s_full + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::tmem_slot_off);
+
+  if (P.counts && int(blockIdx.x) >= P.counts[0]) return;  // past a device plan's items
+  Item it;
+  it.load(P, blockIdx.x);
+  const int G = P.group, bs = P.block_size;
+  const int prefix = it.L - it.qlen;
+  if (P.mask_type == PA_MASK_NORM_COMPRESS && it.nrows > 0) {
+    // causal trim, as in the decode kernel: keys past the last row's position
+    // carry the mask's fill for every row of the tile
+    const int pmax = prefix + (it.r0 + it.nrows - 1) / G;
+    it.tok1 = max(it.tok0, min(it.tok1, pmax + 1));
+  }
+  const int ntok = it.tok1 - it.tok0;
+  const int ntiles = ntok > 0 ? (ntok + kPfTok - 1) / kPfTok : 0;
+  const int sigma = it.L > PA_COMPRESS_MASK_SIZE ? it.L - PA_COMPRESS_MASK_SIZE : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < kPfKSlots; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+    }
+    for (int s = 0; s < kPfVSlots; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 4);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&pv_done[b], 1);
+    }
+    mbar_init(qk_done, 1);
+    mbar_init(o_done, 1);
+    mbar_init(q_ready, 4);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_s = tmem;        // S buffer b: columns [128 b, 128 b + 128)
+  const uint32_t tmem_o = tmem + 256;  // O: columns [256, 256 + HD)
+
+  if (warp == 0) {
+    // ================= TMA producer (lane 0) =================
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const int32_t* bt_row = P.block_tables + int64_t(it.b) * P.max_blocks_per_seq;
+      const int box_rows = bs < kPfTok ? bs : kPfTok;
+      const int pieces = kPfTok / box_rows;
+      const int kz = it.kvh * H2;                              // K: 64-dim blocks of this head
+      const int vz = it.kvh * ((P.kv_shared ? P.hk : HD) / 64);  // V (shared: over the K rows)
+      int kiss = 0, viss = 0;
+      bool ok = true;
+      for (int n = 0; n < ntiles && ok; ++n) {
+        const int t0 = it.tok0 + n * kPfTok;
+        int npieces = 0;
+        for (int pc = 0; pc < pieces; ++pc) {
+          const int tok = t0 + pc * box_rows;
+          if (tok >= it.tok1) break;
+          const int ph = bt_row[tok / bs];
+          if (ph < 0 || ph >= P.num_blocks) {
+            set_status(P.status, PA_STATUS_BIT_BLOCK_INDEX);
+            continue;
+          }
+          ++npieces;
+        }
+        const uint32_t bytes = uint32_t(npieces) * box_rows * 128 * H2;
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const int nslots = kv == 0 ? kPfKSlots : kPfVSlots;
+          int& iss = kv == 0 ? kiss : viss;
+          const int slot = iss % nslots;
+          uint64_t* full = kv == 0 ? &kfull[slot] : &vfull[slot];
+          uint64_t* empty = kv == 0 ? &kempty[slot] : &vempty[slot];
+          if (!mbar_wait(empty, ((iss / nslots) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = (kv == 0 ? kring : vring) + slot * Cfg::kSlot;
+          const CUtensorMap* map = kv == 0 ? &tmk : &tmv;
+          const int z0 = kv == 0 ? kz : vz;
+          if (bytes) mbar_arrive_expect_tx(full, bytes); else mbar_arrive(full);
+          for (int pc = 0; pc < pieces; ++pc) {
+            const int tok = t0 + pc * box_rows;
+            if (tok >= it.tok1) break;
+            const int ph = bt_row[tok / bs];
+            if (ph < 0 || ph >= P.num_blocks) continue;
+            const int row = ph * bs + tok % bs;
+            if (box_rows == kPfTok) {
+              // one box: [H2 halves][128 tokens][128 B] = the slot
+              tma_load_3d(dst, map, full, 0, row, z0, pol);
+            } else {
+              for (int h = 0; h < H2; ++h)
+                tma_load_3d(dst + h * kHalfK + pc * box_rows * 128, map, full, 0, row, z0 + h, pol);
+            }
+          }
+          ++iss;
+        }
+      }
+      if (!ok) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
+      for (int i = kiss - kPfKSlots > 0 ? kiss - kPfKSlots : 0; i < kiss; ++i)
+        mbar_wait(&kfull[i % kPfKSlots], (i / kPfKSlots) & 1);
+      for (int i = viss - kPfVSlots > 0 ? viss - kPfVSlots : 0; i < viss; ++i)
+        mbar_wait(&vfull[i % kPfVSlots], (i / kPfVSlots) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    // S(n) = Q . K(n)^T into buffer n & 1, then O += P(n-1) . V(n-1).
+    bool ok = true;
+    const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
+    const uint32_t k_addr = smem_u32(kring), v_addr = smem_u32(vring);
+    if (ntiles > 0 && !warp_wait(q_ready, 0, lane)) ok = false;
+    auto pv = [&](int m) -> bool {  // O += P(m) . V(m)
+      const int pb = m % kPfPBufs, vs = m % kPfVSlots;
+      if (!warp_wait(&p_full[pb], (m / kPfPBufs) & 1, lane)) return false;
+      if (!warp_wait(&vfull[vs], (m / kPfVSlots) & 1, lane)) return false;
+      const int nvalid = min(kPfTok, it.tok1 - (it.tok0 + m * kPfTok));
+      if (nvalid < kPfTok) {
+        // V rows past the range may hold anything (NaN included): zero them
+        uint8_t* vb = vring + vs * Cfg::kSlot;
+        const int per = (kPfTok - nvalid) * 8;  // 16-byte chunks per half
+        for (int idx = lane; idx < H2 * per; idx += 32) {
+          const int h = idx / per, rem = idx % per;
+          *reinterpret_cast<uint4*>(vb + h * kHalfK + (nvalid + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < kPfTok / 16; ++k) {
+          // A = P (rows x tokens, K-major: 64-token halves of 128 B rows)
+          const uint64_t a = smem_desc(p_addr + pb * Cfg::kP + (k >> 2) * kHalfP + (k & 3) * 32, 16, 1024);
+          // B = V (tokens x dims, MN-major: 64-dim halves kHalfK apart)
+          const uint64_t b = smem_desc(v_addr + vs * Cfg::kSlot + k * 2048, kHalfK, 1024);
+          tc_mma(tmem_o, a, b, kIdescPV, (m | k) != 0);
+        }
+        tc_commit(&vempty[vs]);
+        tc_commit(&pv_done[pb]);
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int n = 0; n < ntiles && ok; ++n) {
+      const int ks = n % kPfKSlots;
+      if (n >= 2 && !warp_wait(&s_free[n & 1], ((n >> 1) - 1) & 1, lane)) { ok = false; break; }
+      if (!warp_wait(&kfull[ks], (n / kPfKSlots) & 1, lane)) { ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < H2; ++h) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t a = smem_desc(q_addr + h * kHalfQ + k * 32, 16, 1024);
+            const uint64_t b = smem_desc(k_addr + ks * Cfg::kSlot + h * kHalfK + k * 32, 16, 1024);
+            tc_mma(tmem_s + (n & 1) * 128, a, b, kIdescQK, (h | k) != 0);
+          }
+        }
+        tc_commit(&kempty[ks]);
+        tc_commit(&s_full[n & 1]);
+      }
+      __syncwarp();
+      if (n >= 1 && !pv(n - 1)) { ok = false; break; }
+    }
+    if (ok && ntiles > 0 && !pv(ntiles - 1)) ok = false;
+    if (!ok && lane == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
+    if (lane == 0) {
+      tc_commit(qk_done);
+      tc_commit(o_done);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ================= softmax warps 4-7: one query row per thread =================
+    const int quarter = warp & 3;
+    const bool active = lane < 16;
+    const int r = quarter * 16 + lane;  // row of the tile (active lanes)
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    const bool row_ok = active && r < it.nrows;
+    const int rr = it.r0 + r;
+    const int qi = row_ok ? rr / G : 0;  // query token of the row
+    const int p_row = prefix + qi;       // its position
+    const float slope = (row_ok && P.mask_type == PA_MASK_ALIBI)
+                            ? P.alibi_slopes[it.kvh * G + rr % G] * kLog2e : 0.f;
+    // Q tile: rows r, 64-dim halves, swizzled; 128 threads, 16-byte chunks
+    {
+      const int st = tid - 128;
+      constexpr int kChunks = kPfRows * (HD / 8);
+#pragma unroll
+      for (int k = 0; k < kChunks / 128; ++k) {
+        const int idx = st + k * 128;
+        const int row = idx / (HD / 8), c = idx % (HD / 8);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < it.nrows) {
+          const int rq = it.r0 + row;
+          v = *reinterpret_cast<const uint4*>(
+              P.query + (int64_t(it.q_start + rq / G) * P.num_heads + it.kvh * G + rq % G) * HD + c * 8);
+        }
+        *reinterpret_cast<uint4*>(q_s + (c >> 3) * kHalfQ + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v;
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+    }
+    float m_ref = -INFINITY;  // reference max of the row (base 2)
+    float l = 0.f;            // sum of exp2(s - m_ref) over the keys so far
+    bool ok = true;
+    for (int n = 0; n < ntiles; ++n) {
+      if (!warp_wait(&s_full[n & 1], (n >> 1) & 1, lane)) { ok = false; break; }
+      tc_fence_after();
+      // Pass 1, 32 columns at a time: scores in base 2 with the bias, written
+      // back into the S buffer, and the tile's row max.
+      const uint32_t sbuf = tmem_s + (n & 1) * 128 + lane_base;
+      const int j0 = it.tok0 + n * kPfTok;  // key of column 0
+      const bool diag = P.mask_type == PA_MASK_NORM_COMPRESS && row_ok && j0 + kPfTok - 1 > p_row;
+      const int mr = min(max(p_row - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
+      float tmax = -INFINITY;
+#pragma unroll 1
+      for (int cc = 0; cc < kPfTok / 32; ++cc) {
+        float x[32];
+        tmem_ld32(sbuf + cc * 32, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int j = j0 + cc * 32 + i;
+          float v = x[i] * P.scale_log2;
+          if (P.mask_type == PA_MASK_ALIBI) {
+            v += slope * float(j - p_row);
+          } else if (P.mask_type == PA_MASK_NORM) {
+            if (row_ok && j < it.tok1) v += norm_mask_log2(P, it.b, qi, j);
+          } else if (diag && j > p_row && j < it.tok1) {
+            // above this row's diagonal: the compressed mask's value
+            const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
+            v += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
+          }
+          v = (j < it.tok1) ? v : -INFINITY;
+          x[i] = v;
+          tmax = fmaxf(tmax, v);
+        }
+        tmem_st32(sbuf + cc * 32, x);
+      }
+      tmem_wait_st();
+      // move the reference only when a score passes it by more than 2^8
+      const bool grow = tmax > m_ref + kTcRescaleThreshold;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m_ref - tmax);  // 0 on the first tile
+        m_ref = tmax;
+        l *= alpha;
+      }
+      // P buffer n % 2 was read by PV(n - 2); a rescale of O needs PV(n - 1)
+      const bool any_grow = __any_sync(0xffffffffu, grow && row_ok);
+      bool w = true;
+      if (any_grow && n >= 1) w = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1);
+      if (n >= 2) w = w && mbar_wait(&pv_done[n & 1], ((n - 2) >> 1) & 1);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc_fence_after();
+      // Pass 2: probabilities straight into P (fp16): row r, 16-byte chunks of
+      // 8 tokens, 64-token halves, swizzled. Then the S buffer is free.
+      float psum = 0.f;
+      uint8_t* pb = p_s + (n & 1) * Cfg::kP;
+#pragma unroll 1
+      for (int cc = 0; cc < kPfTok / 32; ++cc) {
+        float x[32];
+        tmem_ld32(sbuf + cc * 32, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float e[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            e[i] = ex2(x[q8 * 8 + i] - m_ref);
+            psum += e[i];
+          }
+          uint4 pk;
+          pk.x = pack_half2(e[0], e[1]);
+          pk.y = pack_half2(e[2], e[3]);
+          pk.z = pack_half2(e[4], e[5]);
+          pk.w = pack_half2(e[6], e[7]);
+          const int c8 = cc * 4 + q8;
+          if (active)
+            *reinterpret_cast<uint4*>(pb + (c8 >> 3) * kHalfP + r * 128 + (((c8 & 7) ^ (r & 7)) << 4)) = pk;
+        }
+      }
+      l += psum;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[n & 1]);
+      if (any_grow && n >= 1) {
+        // rescale this warp's O rows (rows that did not grow use alpha = 1)
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          float o[32];
+          tmem_ld32(tmem_o + c * 32 + lane_base, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tmem_o + c * 32 + lane_base, o);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[n & 1]);
+    }
+    if (!ok && lane == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
+    launch_dependents();
+    const bool got = ok && warp_wait(o_done, 0, lane);
+    const bool partial = it.slot >= 0;
+    const bool fits = !partial || int64_t(it.slot) + it.nrows <= P.part_rows_cap;
+    if (!fits && r == 0) set_status(P.status, PA_STATUS_BIT_WORKSPACE);
+    if (got && fits) {
+      tc_fence_after();
+      const float inv = ntiles > 0 ? 1.f / l : 0.f;
+      // this thread's row: HD values, 32 columns at a time
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float o[32];
+        tmem_ld32(tmem_o + c * 32 + lane_base, o);
+        tmem_wait_ld();
+        if (!row_ok) continue;
+        if (partial) {
+          float4* dst = reinterpret_cast<float4*>(P.part_o + (int64_t(it.slot) + r) * HD + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = ntiles > 0 ? make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                              o[4 * i + 3] * inv)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(
+              P.out + (int64_t(it.q_start + qi) * P.num_heads + it.kvh * G + rr % G) * HD + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 pk;
+            pk.x = pack_half2(o[8 * i + 0] * inv, o[8 * i + 1] * inv);
+            pk.y = pack_half2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
+            pk.z = pack_half2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
+            pk.w = pack_half2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
+            dst[i] = pk;
+          }
+        }
+      }
+      if (partial && row_ok)
+        P.part_lse[it.slot + r] = ntiles > 0 ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+  // ---- teardown: every tcgen05 op has completed before TMEM is freed
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) {
+      mbar_wait(qk_done, 0);
+      mbar_wait(o_done, 0);
+    }
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols));
+  }
+}
+
+cudaError_t launch_pf(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdParams& P,
+                      int64_t n_items, cudaStream_t stream);
+
+}  // namespace pa

@@ -206,6 +206,19 @@ TC_CASES = {
                                               num_heads=8, kv_heads=2, head_size_k=128,
                                               block_size=32, mask_type=W.MASK_NORM_COMPRESS,
                                               seed=41),
+    # many-row tiles (prefill kernel): head size 64, ALiBi, 16-token blocks
+    "pf_hd64_alibi_bs16": lambda: W.make_workload("pf64", context_lens=[333, 90], q_seqlens=[40, 90],
+                                                  num_heads=8, kv_heads=4, head_size_k=64,
+                                                  block_size=16, mask_type=W.MASK_ALIBI, seed=42),
+    # MASK_TYPE_NORM on the prefill kernel (q = 100 of L = 260, 2 heads per kv head)
+    "pf_norm": lambda: W.make_workload("pfn", context_lens=[260, 100], q_seqlens=[100, 60],
+                                       num_heads=4, kv_heads=2, head_size_k=128, block_size=32,
+                                       mask_type=W.MASK_NORM, seed=43),
+    # no mask, splits across 128-token tiles, shared-KV cache (V = K)
+    "pf_shared_split": lambda: W.make_workload("pfs", context_lens=[700, 1300], q_seqlens=[70, 33],
+                                               num_heads=4, kv_heads=2, head_size_k=128,
+                                               block_size=64, seed=44, shared_kv=True,
+                                               chunk_blocks=4),
     # MASK_TYPE_NORM on the tensor-core path: 16 heads x 2 tokens per kv head
     "tc_norm": lambda: W.make_workload("tcn", context_lens=[300, 1200], q_seqlens=[2, 1],
                                        num_heads=16, kv_heads=1, head_size_k=128, block_size=64,
@@ -263,11 +276,11 @@ def sample_rows(w, k, seed):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["gqa_decode", "spec_decode", "alibi_decode", "mqa_split",
-                                  "mla_decode"])
+                                  "mla_decode", "prefill_causal"])
 def test_full_size_sampled(oracle_mod, name):
     w = W.NAMED[name]()
     got, db = run_gpu(w)
-    pick, rows = sample_rows(w, 2 if name == "mqa_split" else 6, 99)
+    pick, rows = sample_rows(w, {"mqa_split": 2, "prefill_causal": 1}.get(name, 6), 99)
     ref, _ = oracle_mod.attention(w, subset=pick, threads=CORES)
     compare(got, ref, rows)
     # every output row is finite (NaN-poisoned tail slots and spare blocks never read)
