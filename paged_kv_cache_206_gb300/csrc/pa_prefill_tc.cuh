@@ -4,20 +4,22 @@
 // decode kernels (PagedAttentionOperation semantics; task list and FlashDecode
 // merge of the SparseAttnSharedkvMetadata page); a different tile shape.
 //
-// One CTA per work item (64 query rows), 128-token key tiles, 8 warps:
+// One CTA per work item (64 query rows), 128-token key tiles, 12 warps:
 //   warp 0     TMA producer: K and V of each key tile (3-D boxes, 128-byte
 //              swizzle) into a 3-slot K ring and a 2-slot V ring.
 //   warp 1     allocates TMEM; one thread issues S = Q . K^T (M=64 rows,
 //              N=128 tokens, K-major operands; S double-buffered in TMEM),
 //              then O += P . V for the previous tile (M=64, N=hd; A = P
 //              K-major, B = V MN-major; O accumulates in TMEM).
-//   warps 4-7  softmax, one query row per thread (M=64 puts rows 16q..16q+15
-//              in lanes 0-15 of TMEM lane quarter q): the row's scores come
-//              from TMEM in 32-column loads, so max and sum need no exchange
-//              between threads. The reference max is moved (and O rescaled in
-//              TMEM) only when a score exceeds it by more than 2^8. P (fp16)
-//              goes to shared memory, double-buffered, in the K-major
-//              swizzled layout the PV MMA reads.
+//   warps 4-11 softmax in two groups of four that take alternate key tiles,
+//              each with its own running max, sum and O accumulator (merged
+//              per row at the end); one query row per thread (M=64 puts rows
+//              16q..16q+15 in lanes 0-15 of TMEM lane quarter q): the row's
+//              scores come from TMEM in 32-column loads, so max and sum need
+//              no exchange between threads. The reference max is moved (and
+//              O rescaled in TMEM) only when a score exceeds it by more than
+//              2^8. P (fp16) goes to shared memory in the K-major swizzled
+//              layout the PV MMA reads; each group has its own P buffer.
 //   warps 2-3  no role.
 // With the compressed causal mask an item stops after its last query row's
 // position, and only the keys above the diagonal read the mask. Every wait is
@@ -31,7 +33,7 @@ namespace pa {
 
 constexpr int kPfTok = 128;      // key tokens per tile (N of S = Q . K^T)
 constexpr int kPfRows = 64;      // query rows per tile (M of both MMAs)
-constexpr int kPfThreads = 256;  // 8 warps
+constexpr int kPfThreads = 384;  // 12 warps
 constexpr int kPfKSlots = 3;
 constexpr int kPfVSlots = 2;
 constexpr int kPfPBufs = 2;
@@ -48,7 +50,8 @@ struct PfCfg {
   static constexpr uint32_t v_off = k_off + kPfKSlots * kSlot;
   static constexpr uint32_t bars_off = v_off + kPfVSlots * kSlot;
   static constexpr int kBars = 2 * (kPfKSlots + kPfVSlots) + 12;
-  static constexpr uint32_t tmem_slot_off = bars_off + kBars * 8;
+  static constexpr uint32_t xchg_off = bars_off + kBars * 8;  // [2][64] fp32 row merge
+  static constexpr uint32_t tmem_slot_off = xchg_off + 2 * kPfRows * 4;
   static constexpr uint32_t bytes = tmem_slot_off + 16 + 1024;
   static_assert(bytes <= kTcMaxSmem, "shared memory");
 };
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_s = tmem;        // S buffer b: columns [128 b, 128 b + 128)
-  const uint32_t tmem_o = tmem + 256;  // O: columns [256, 256 + HD)
+  const uint32_t tmem_o = tmem + 256;  // O of group g: columns [256 + 128 g, 256 + 128 g + HD)
 
   if (warp == 0) {
     // ================= TMA producer (lane 0) =================
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
     const uint32_t k_addr = smem_u32(kring), v_addr = smem_u32(vring);
     if (ntiles > 0 && !warp_wait(q_ready, 0, lane)) ok = false;
     auto pv = [&](int m) -> bool {  // O += P(m) . V(m)
-      const int pb = m % kPfPBufs, vs = m % kPfVSlots;
+      const int pb = m & 1, vs = m % kPfVSlots;  // P buffer and O accumulator of tile m's group
       if (!warp_wait(&p_full[pb], (m / kPfPBufs) & 1, lane)) return false;
       if (!warp_wait(&vfull[vs], (m / kPfVSlots) & 1, lane)) return false;
       const int nvalid = min(kPfTok, it.tok1 - (it.tok0 + m * kPfTok));
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
           const uint64_t a = smem_desc(p_addr + pb * Cfg::kP + (k >> 2) * kHalfP + (k & 3) * 32, 16, 1024);
           // B = V (tokens x dims, MN-major: 64-dim halves kHalfK apart)
           const uint64_t b = smem_desc(v_addr + vs * Cfg::kSlot + k * 2048, kHalfK, 1024);
-          tc_mma(tmem_o, a, b, kIdescPV, (m | k) != 0);
+          tc_mma(tmem_o + pb * 128, a, b, kIdescPV, ((m >> 1) | k) != 0);
         }
         tc_commit(&vempty[vs]);
         tc_commit(&pv_done[pb]);
@@ -267,19 +270,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ================= softmax warps 4-7: one query row per thread =================
+    // ================= softmax: group g (warps 4-7 / 8-11) takes tiles n = g mod 2 =====
+    // Each group keeps its own running max, sum and O accumulator (TMEM
+    // columns 256 + 128 g); the two states of a row are merged at the end.
+    const int grp = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const bool active = lane < 16;
     const int r = quarter * 16 + lane;  // row of the tile (active lanes)
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    const uint32_t o_mine = tmem_o + grp * 128 + lane_base;
     const bool row_ok = active && r < it.nrows;
     const int rr = it.r0 + r;
     const int qi = row_ok ? rr / G : 0;  // query token of the row
     const int p_row = prefix + qi;       // its position
     const float slope = (row_ok && P.mask_type == PA_MASK_ALIBI)
                             ? P.alibi_slopes[it.kvh * G + rr % G] * kLog2e : 0.f;
-    // Q tile: rows r, 64-dim halves, swizzled; 128 threads, 16-byte chunks
-    {
+    if (grp == 0) {
+      // Q tile: rows r, 64-dim halves, swizzled; 128 threads, 16-byte chunks
       const int st = tid - 128;
       constexpr int kChunks = kPfRows * (HD / 8);
 #pragma unroll
@@ -298,63 +305,99 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
     }
-    float m_ref = -INFINITY;  // reference max of the row (base 2)
-    float l = 0.f;            // sum of exp2(s - m_ref) over the keys so far
+    float m_ref = -INFINITY;  // reference max of the row over this group's tiles (base 2)
+    float l = 0.f;            // sum of exp2(s - m_ref) over those keys
     bool ok = true;
-    for (int n = 0; n < ntiles; ++n) {
-      if (!warp_wait(&s_full[n & 1], (n >> 1) & 1, lane)) { ok = false; break; }
+    for (int n = grp; n < ntiles; n += 2) {
+      const int b = n & 1;  // = grp: S, P and O buffers of this group
+      if (!warp_wait(&s_full[b], (n >> 1) & 1, lane)) { ok = false; break; }
       tc_fence_after();
       // Pass 1, 32 columns at a time: scores in base 2 with the bias, written
       // back into the S buffer, and the tile's row max.
-      const uint32_t sbuf = tmem_s + (n & 1) * 128 + lane_base;
+      const uint32_t sbuf = tmem_s + b * 128 + lane_base;
       const int j0 = it.tok0 + n * kPfTok;  // key of column 0
-      const bool diag = P.mask_type == PA_MASK_NORM_COMPRESS && row_ok && j0 + kPfTok - 1 > p_row;
-      const int mr = min(max(p_row - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
+      const int jend = it.tok1 - j0;       // columns at or past this are outside the range
       float tmax = -INFINITY;
+      // (tcgen05.ld / st are warp-collective: the branch below must be taken by
+      // the whole warp, so the test is whether any row of the warp needs it)
+      const bool diag_row = row_ok && j0 + kPfTok - 1 > p_row;
+      if (P.mask_type == PA_MASK_NORM_COMPRESS && __any_sync(0xffffffffu, diag_row)) {
+        // a tile reaching above some row's diagonal: read the mask there
+        const int mr = min(max(p_row - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
 #pragma unroll 1
-      for (int cc = 0; cc < kPfTok / 32; ++cc) {
-        float x[32];
-        tmem_ld32(sbuf + cc * 32, x);
-        tmem_wait_ld();
+        for (int cc = 0; cc < kPfTok / 32; ++cc) {
+          float x[32];
+          tmem_ld32(sbuf + cc * 32, x);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int j = j0 + cc * 32 + i;
-          float v = x[i] * P.scale_log2;
-          if (P.mask_type == PA_MASK_ALIBI) {
-            v += slope * float(j - p_row);
-          } else if (P.mask_type == PA_MASK_NORM) {
-            if (row_ok && j < it.tok1) v += norm_mask_log2(P, it.b, qi, j);
-          } else if (diag && j > p_row && j < it.tok1) {
-            // above this row's diagonal: the compressed mask's value
-            const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
-            v += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
+          for (int i = 0; i < 32; ++i) {
+            const int c = cc * 32 + i, j = j0 + c;
+            float v = x[i] * P.scale_log2;
+            if (diag_row && j > p_row && c < jend) {
+              const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
+              v += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
+            }
+            v = c < jend ? v : -INFINITY;
+            x[i] = v;
+            tmax = fmaxf(tmax, v);
           }
-          v = (j < it.tok1) ? v : -INFINITY;
-          x[i] = v;
-          tmax = fmaxf(tmax, v);
+          tmem_st32(sbuf + cc * 32, x);
         }
-        tmem_st32(sbuf + cc * 32, x);
+      } else if (P.mask_type == PA_MASK_ALIBI || P.mask_type == PA_MASK_NORM) {
+        const bool alibi = P.mask_type == PA_MASK_ALIBI;
+#pragma unroll 1
+        for (int cc = 0; cc < kPfTok / 32; ++cc) {
+          float x[32];
+          tmem_ld32(sbuf + cc * 32, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = cc * 32 + i, j = j0 + c;
+            float v = x[i] * P.scale_log2;
+            if (alibi) v += slope * float(j - p_row);
+            else if (row_ok && c < jend) v += norm_mask_log2(P, it.b, qi, j);
+            v = c < jend ? v : -INFINITY;
+            x[i] = v;
+            tmax = fmaxf(tmax, v);
+          }
+          tmem_st32(sbuf + cc * 32, x);
+        }
+      } else {
+        // no bias (or a tile wholly on or below the diagonal)
+#pragma unroll 1
+        for (int cc = 0; cc < kPfTok / 32; ++cc) {
+          float x[32];
+          tmem_ld32(sbuf + cc * 32, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float v = cc * 32 + i < jend ? x[i] * P.scale_log2 : -INFINITY;
+            x[i] = v;
+            tmax = fmaxf(tmax, v);
+          }
+          tmem_st32(sbuf + cc * 32, x);
+        }
       }
       tmem_wait_st();
       // move the reference only when a score passes it by more than 2^8
       const bool grow = tmax > m_ref + kTcRescaleThreshold;
       float alpha = 1.f;
       if (grow) {
-        alpha = ex2(m_ref - tmax);  // 0 on the first tile
+        alpha = ex2(m_ref - tmax);  // 0 on this group's first tile
         m_ref = tmax;
         l *= alpha;
       }
-      // P buffer n % 2 was read by PV(n - 2); a rescale of O needs PV(n - 1)
-      const bool any_grow = __any_sync(0xffffffffu, grow && row_ok);
-      bool w = true;
-      if (any_grow && n >= 1) w = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1);
-      if (n >= 2) w = w && mbar_wait(&pv_done[n & 1], ((n - 2) >> 1) & 1);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      // this group's previous PV (tile n - 2) read P buffer b and wrote O: both
+      // the P rewrite and a rescale of O wait for it
+      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[b], ((n - 2) >> 1) & 1))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       // Pass 2: probabilities straight into P (fp16): row r, 16-byte chunks of
       // 8 tokens, 64-token halves, swizzled. Then the S buffer is free.
       float psum = 0.f;
-      uint8_t* pb = p_s + (n & 1) * Cfg::kP;
+      uint8_t* pb = p_s + b * Cfg::kP;
 #pragma unroll 1
       for (int cc = 0; cc < kPfTok / 32; ++cc) {
         float x[32];
@@ -381,64 +424,77 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
       l += psum;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[n & 1]);
-      if (any_grow && n >= 1) {
-        // rescale this warp's O rows (rows that did not grow use alpha = 1)
+      if (lane == 0) mbar_arrive(&s_free[b]);
+      if (n >= 2 && __any_sync(0xffffffffu, grow && row_ok)) {
+        // rescale this warp's rows of this group's O (rows that did not grow use 1)
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
           float o[32];
-          tmem_ld32(tmem_o + c * 32 + lane_base, o);
+          tmem_ld32(o_mine + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tmem_o + c * 32 + lane_base, o);
+          tmem_st32(o_mine + c * 32, o);
         }
         tmem_wait_st();
       }
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[n & 1]);
+      if (lane == 0) mbar_arrive(&p_full[b]);
     }
     if (!ok && lane == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
     launch_dependents();
-    const bool got = ok && warp_wait(o_done, 0, lane);
-    const bool partial = it.slot >= 0;
-    const bool fits = !partial || int64_t(it.slot) + it.nrows <= P.part_rows_cap;
-    if (!fits && r == 0) set_status(P.status, PA_STATUS_BIT_WORKSPACE);
-    if (got && fits) {
-      tc_fence_after();
-      const float inv = ntiles > 0 ? 1.f / l : 0.f;
-      // this thread's row: HD values, 32 columns at a time
+    // ---- merge the two groups' states per row, then O / l
+    float* xm = reinterpret_cast<float*>(smem + Cfg::xchg_off);  // [2][64]: group 1's m and l
+    if (grp == 1 && active) {
+      xm[r] = m_ref;
+      xm[kPfRows + r] = l;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // the 8 softmax warps
+    if (grp == 0) {
+      const bool got = ok && warp_wait(o_done, 0, lane);
+      const bool partial = it.slot >= 0;
+      const bool fits = !partial || int64_t(it.slot) + it.nrows <= P.part_rows_cap;
+      if (!fits && r == 0) set_status(P.status, PA_STATUS_BIT_WORKSPACE);
+      if (got && fits) {
+        tc_fence_after();
+        const bool two = ntiles >= 2;  // group 1 ran (and wrote its O)
+        const float m1 = two ? xm[r] : -INFINITY, l1 = two ? xm[kPfRows + r] : 0.f;
+        const float mm = fmaxf(m_ref, m1);
+        const float a0 = ntiles > 0 ? ex2(m_ref - mm) : 0.f, a1 = two ? ex2(m1 - mm) : 0.f;
+        const float lt = l * a0 + l1 * a1;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const float w0 = a0 * inv, w1 = a1 * inv;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
-        float o[32];
-        tmem_ld32(tmem_o + c * 32 + lane_base, o);
-        tmem_wait_ld();
-        if (!row_ok) continue;
-        if (partial) {
-          float4* dst = reinterpret_cast<float4*>(P.part_o + (int64_t(it.slot) + r) * HD + c * 32);
+        for (int c = 0; c < HD / 32; ++c) {
+          float o[32], o1[32];
+          tmem_ld32(tmem_o + c * 32 + lane_base, o);
+          if (two) tmem_ld32(tmem_o + 128 + c * 32 + lane_base, o1);
+          tmem_wait_ld();
+          if (!row_ok) continue;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = ntiles > 0 ? make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                              o[4 * i + 3] * inv)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(
-              P.out + (int64_t(it.q_start + qi) * P.num_heads + it.kvh * G + rr % G) * HD + c * 32);
+          for (int i = 0; i < 32; ++i) o[i] = (ntiles > 0 ? o[i] * w0 : 0.f) + (two ? o1[i] * w1 : 0.f);
+          if (partial) {
+            float4* dst = reinterpret_cast<float4*>(P.part_o + (int64_t(it.slot) + r) * HD + c * 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 pk;
-            pk.x = pack_half2(o[8 * i + 0] * inv, o[8 * i + 1] * inv);
-            pk.y = pack_half2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
-            pk.z = pack_half2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
-            pk.w = pack_half2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
-            dst[i] = pk;
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(
+                P.out + (int64_t(it.q_start + qi) * P.num_heads + it.kvh * G + rr % G) * HD + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 pk;
+              pk.x = pack_half2(o[8 * i + 0], o[8 * i + 1]);
+              pk.y = pack_half2(o[8 * i + 2], o[8 * i + 3]);
+              pk.z = pack_half2(o[8 * i + 4], o[8 * i + 5]);
+              pk.w = pack_half2(o[8 * i + 6], o[8 * i + 7]);
+              dst[i] = pk;
+            }
           }
         }
+        if (partial && row_ok) P.part_lse[it.slot + r] = lt > 0.f ? (mm + log2f(lt)) * kLn2 : -INFINITY;
       }
-      if (partial && row_ok)
-        P.part_lse[it.slot + r] = ntiles > 0 ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
     }
   }
   // ---- teardown: every tcgen05 op has completed before TMEM is freed
