@@ -91,8 +91,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::tmem_slot_off);
 
   if (P.counts && int(blockIdx.x) >= P.counts[0]) return;  // past a device plan's items
+  // Items run last to first: with the causal mask the later row tiles of a
+  // sequence meet more keys, so the longest items start first and the last
+  // wave holds the short ones.
+  const int n_items = P.counts ? P.counts[0] : int(gridDim.x);
   Item it;
-  it.load(P, blockIdx.x);
+  it.load(P, n_items - 1 - int(blockIdx.x));
   const int G = P.group, bs = P.block_size;
   const int prefix = it.L - it.qlen;
   if (P.mask_type == PA_MASK_NORM_COMPRESS && it.nrows > 0) {
