@@ -291,7 +291,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   constexpr int kKSlots = Cfg::kKSlots, kVSlots = Cfg::kVSlots;
   constexpr int RH = NR / 2;  // rows per softmax thread (two warps per lane quarter)
   constexpr uint32_t kIdescQK = mma_idesc(64, NR, 0, 0);
-  constexpr uint32_t kIdescPV = mma_idesc(128, kTcRows, 1, 1);
+  // PV reads the first NR columns of each 128-byte P^T row (the tile's rows)
+  constexpr uint32_t kIdescPV = mma_idesc(128, NR, 1, 1);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
