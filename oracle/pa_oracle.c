@@ -193,7 +193,8 @@ static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 /*
  * The work-list rule, restated from its written definition:
- *   tile height    TR = G * maxq if that is at most 8, else 64
+ *   tile height    TR = G * maxq if that is at most 8; else 128 if G * maxq > 64
+ *                  and hk = hv in {64, 128}; else 64
  *   tiles          QT_b = ceil(G * q_b / TR)
  *   blocks         NB_b = ceil(L_b / bs)
  *   chunk          c = chunk_blocks if positive, else
@@ -215,7 +216,9 @@ int oracle_plan(int batch, int num_heads, int kv_heads, int hk, int hv, int bloc
                 int32_t* comb, int64_t comb_cap, int64_t* n_comb, int64_t* n_partial_rows) {
   const int64_t G = num_heads / kv_heads;
   const int64_t maxq = max_seqlen_q > 0 ? max_seqlen_q : 1;
-  const int64_t TR = (G * maxq <= 8) ? G * maxq : 64;
+  int64_t TR = 64;
+  if (G * maxq <= 8) TR = G * maxq;
+  else if (G * maxq > 64 && hk == hv && (hk == 64 || hk == 128)) TR = 128;
   int64_t c;
   if (chunk_blocks > 0) {
     c = chunk_blocks;

@@ -35,6 +35,7 @@ PA_COMBINE_INTS = 4
 PA_STATUS_BYTES = 256
 PA_FMA_MAX_ROWS = 8
 PA_TC_TILE_ROWS = 64
+PA_PF_TILE_ROWS = 128
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_plan", "pa_forward", "pa_forward_noalloc", "pa_plan_bounds", "pa_plan_device",
@@ -288,7 +289,13 @@ def list_capacity(cfg: pa_config) -> tuple[int, int]:
     ceil(NB / c) <= NB / c + 1, number at most 8 * num_sms + B * Hk * QT.
     """
     rows = (cfg.num_heads // cfg.kv_heads) * max(1, cfg.max_seqlen_q)
-    tr = rows if rows <= PA_FMA_MAX_ROWS else PA_TC_TILE_ROWS
+    pf_heads = cfg.head_size_k == cfg.head_size_v and cfg.head_size_k in (64, 128)
+    if rows <= PA_FMA_MAX_ROWS:
+        tr = rows
+    elif rows > PA_TC_TILE_ROWS and pf_heads:
+        tr = PA_PF_TILE_ROWS
+    else:
+        tr = PA_TC_TILE_ROWS
     tiles = cfg.batch * cfg.kv_heads * (-(-rows // tr))
     if cfg.chunk_blocks > 0:
         items = tiles * (-(-cfg.max_blocks_per_seq // cfg.chunk_blocks))

@@ -249,7 +249,7 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
       case 4: err = launch_fma<4>(tmk, tmv, P, n_items, stream); break;
       default: err = launch_fma<8>(tmk, tmv, P, n_items, stream); break;
     }
-  } else if (int64_t(P.group) * max_q(c) > PA_TC_TILE_ROWS && pf_supported(hk, hv)) {
+  } else if (TR == PA_PF_TILE_ROWS) {
     // rows meet many keys (prefill, or more than one 64-row tile per kv head):
     // 128-token key tiles, boxes of min(block_size, 128) tokens, both 64-dim
     // halves in one box at 128

@@ -22,7 +22,9 @@ inline int64_t max_q(const pa_config& c) { return c.max_seqlen_q > 0 ? c.max_seq
 inline int64_t tile_rows(const pa_config& c) {
   const int64_t g = c.num_heads / c.kv_heads;
   const int64_t r = g * max_q(c);
-  return r <= PA_FMA_MAX_ROWS ? r : PA_TC_TILE_ROWS;
+  if (r <= PA_FMA_MAX_ROWS) return r;
+  const bool pf_heads = c.head_size_k == c.head_size_v && (c.head_size_k == 64 || c.head_size_k == 128);
+  return (r > PA_TC_TILE_ROWS && pf_heads) ? PA_PF_TILE_ROWS : PA_TC_TILE_ROWS;
 }
 
 struct WorkspaceLayout {

@@ -4,17 +4,18 @@
 // decode kernels (PagedAttentionOperation semantics; task list and FlashDecode
 // merge of the SparseAttnSharedkvMetadata page); a different tile shape.
 //
-// One CTA per work item (64 query rows), 128-token key tiles, 12 warps:
+// One CTA per work item (a 128-row tile: the work list uses 128-row tiles
+// for these launches), 128-token key tiles, 12 warps:
 //   warp 0     TMA producer: K and V of each key tile (3-D boxes, 128-byte
-//              swizzle) into a 3-slot K ring and a 2-slot V ring.
-//   warp 1     allocates TMEM; one thread issues S = Q . K^T (M=64 rows,
+//              swizzle) into 2-slot K and V rings.
+//   warp 1     allocates TMEM; one thread issues S = Q . K^T (M=128 rows,
 //              N=128 tokens, K-major operands; S double-buffered in TMEM),
-//              then O += P . V for the previous tile (M=64, N=hd; A = P
+//              then O += P . V for the previous tile (M=128, N=hd; A = P
 //              K-major, B = V MN-major; O accumulates in TMEM).
 //   warps 4-11 softmax in two groups of four that take alternate key tiles,
 //              each with its own running max, sum and O accumulator (merged
-//              per row at the end); one query row per thread (M=64 puts rows
-//              16q..16q+15 in lanes 0-15 of TMEM lane quarter q): the row's
+//              per row at the end); one query row per thread (TMEM lane m
+//              holds row m of an M=128 accumulator): the row's
 //              scores come from TMEM in 32-column loads, so max and sum need
 //              no exchange between threads. The reference max is moved (and
 //              O rescaled in TMEM) only when a score exceeds it by more than
@@ -32,9 +33,9 @@
 namespace pa {
 
 constexpr int kPfTok = 128;      // key tokens per tile (N of S = Q . K^T)
-constexpr int kPfRows = 64;      // query rows per tile (M of both MMAs)
+constexpr int kPfRows = PA_PF_TILE_ROWS;  // query rows per tile (M of both MMAs)
 constexpr int kPfThreads = 384;  // 12 warps
-constexpr int kPfKSlots = 3;
+constexpr int kPfKSlots = 2;
 constexpr int kPfVSlots = 2;
 constexpr int kPfPBufs = 2;
 
@@ -50,7 +51,7 @@ struct PfCfg {
   static constexpr uint32_t v_off = k_off + kPfKSlots * kSlot;
   static constexpr uint32_t bars_off = v_off + kPfVSlots * kSlot;
   static constexpr int kBars = 2 * (kPfKSlots + kPfVSlots) + 12;
-  static constexpr uint32_t xchg_off = bars_off + kBars * 8;  // [2][64] fp32 row merge
+  static constexpr uint32_t xchg_off = bars_off + kBars * 8;  // [2][rows] fp32 row merge
   static constexpr uint32_t tmem_slot_off = xchg_off + 2 * kPfRows * 4;
   static constexpr uint32_t bytes = tmem_slot_off + 16 + 1024;
   static_assert(bytes <= kTcMaxSmem, "shared memory");
@@ -279,8 +280,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
     // columns 256 + 128 g); the two states of a row are merged at the end.
     const int grp = (warp - 4) >> 2;
     const int quarter = warp & 3;
-    const bool active = lane < 16;
-    const int r = quarter * 16 + lane;  // row of the tile (active lanes)
+    const bool active = true;           // M=128: TMEM lane m holds row m
+    const int r = quarter * 32 + lane;  // row of the tile
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     const uint32_t o_mine = tmem_o + grp * 128 + lane_base;
     const bool row_ok = active && r < it.nrows;
@@ -450,7 +451,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
     if (!ok && lane == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
     launch_dependents();
     // ---- merge the two groups' states per row, then O / l
-    float* xm = reinterpret_cast<float*>(smem + Cfg::xchg_off);  // [2][64]: group 1's m and l
+    float* xm = reinterpret_cast<float*>(smem + Cfg::xchg_off);  // [2][rows]: group 1's m and l
     if (grp == 1 && active) {
       xm[r] = m_ref;
       xm[kPfRows + r] = l;
