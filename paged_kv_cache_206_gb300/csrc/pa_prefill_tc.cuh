@@ -208,66 +208,84 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
     __syncwarp();
   } else if (warp == 1) {
     // ================= MMA issuer =================
-    // S(n) = Q . K(n)^T into buffer n & 1, then O += P(n-1) . V(n-1).
+    // Issues S(n) = Q . K(n)^T (into S buffer n & 1) and O += P(m) . V(m)
+    // (into the O of tile m's group) in whatever order their inputs become
+    // ready, so that one group's softmax never holds back the other's next
+    // QK. Lane 0 polls; the warp follows its verdicts.
     bool ok = true;
     const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
     const uint32_t k_addr = smem_u32(kring), v_addr = smem_u32(vring);
     if (ntiles > 0 && !warp_wait(q_ready, 0, lane)) ok = false;
-    auto pv = [&](int m) -> bool {  // O += P(m) . V(m)
-      const int pb = m & 1, vs = m % kPfVSlots;  // P buffer and O accumulator of tile m's group
-      if (!warp_wait(&p_full[pb], (m / kPfPBufs) & 1, lane)) return false;
-      if (!warp_wait(&vfull[vs], (m / kPfVSlots) & 1, lane)) return false;
-      const int nvalid = min(kPfTok, it.tok1 - (it.tok0 + m * kPfTok));
-      if (nvalid < kPfTok) {
-        // V rows past the range may hold anything (NaN included): zero them
-        uint8_t* vb = vring + vs * Cfg::kSlot;
-        const int per = (kPfTok - nvalid) * 8;  // 16-byte chunks per half
-        for (int idx = lane; idx < H2 * per; idx += 32) {
-          const int h = idx / per, rem = idx % per;
-          *reinterpret_cast<uint4*>(vb + h * kHalfK + (nvalid + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async();
-        __syncwarp();
-      }
-      tc_fence_after();
-      if (lane == 0) {
-#pragma unroll
-        for (int k = 0; k < kPfTok / 16; ++k) {
-          // A = P (rows x tokens, K-major: 64-token halves of 128 B rows)
-          const uint64_t a = smem_desc(p_addr + pb * Cfg::kP + (k >> 2) * kHalfP + (k & 3) * 32, 16, 1024);
-          // B = V (tokens x dims, MN-major: 64-dim halves kHalfK apart)
-          const uint64_t b = smem_desc(v_addr + vs * Cfg::kSlot + k * 2048, kHalfK, 1024);
-          tc_mma(tmem_o + pb * 128, a, b, kIdescPV, ((m >> 1) | k) != 0);
-        }
-        tc_commit(&vempty[vs]);
-        tc_commit(&pv_done[pb]);
-      }
-      __syncwarp();
-      return true;
+    auto ready = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool r = lane == 0 ? mbar_try_wait(bar, parity) : false;
+      return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
     };
-    for (int n = 0; n < ntiles && ok; ++n) {
-      const int ks = n % kPfKSlots;
-      if (n >= 2 && !warp_wait(&s_free[n & 1], ((n >> 1) - 1) & 1, lane)) { ok = false; break; }
-      if (!warp_wait(&kfull[ks], (n / kPfKSlots) & 1, lane)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
+    int nq = 0, np = 0;  // next QK tile, next PV tile
+    long long idle_since = clock64();
+    while (ok && np < ntiles) {
+      bool progressed = false;
+      // QK(nq): its K slot has landed and its S buffer was read (tile nq - 2)
+      if (nq < ntiles && (nq < 2 || ready(&s_free[nq & 1], ((nq >> 1) - 1) & 1)) &&
+          ready(&kfull[nq % kPfKSlots], (nq / kPfKSlots) & 1)) {
+        const int ks = nq % kPfKSlots;
+        tc_fence_after();
+        if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < H2; ++h) {
+          for (int h = 0; h < H2; ++h) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = smem_desc(q_addr + h * kHalfQ + k * 32, 16, 1024);
-            const uint64_t b = smem_desc(k_addr + ks * Cfg::kSlot + h * kHalfK + k * 32, 16, 1024);
-            tc_mma(tmem_s + (n & 1) * 128, a, b, kIdescQK, (h | k) != 0);
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t a = smem_desc(q_addr + h * kHalfQ + k * 32, 16, 1024);
+              const uint64_t b = smem_desc(k_addr + ks * Cfg::kSlot + h * kHalfK + k * 32, 16, 1024);
+              tc_mma(tmem_s + (nq & 1) * 128, a, b, kIdescQK, (h | k) != 0);
+            }
           }
+          tc_commit(&kempty[ks]);
+          tc_commit(&s_full[nq & 1]);
         }
-        tc_commit(&kempty[ks]);
-        tc_commit(&s_full[n & 1]);
+        __syncwarp();
+        ++nq;
+        progressed = true;
       }
-      __syncwarp();
-      if (n >= 1 && !pv(n - 1)) { ok = false; break; }
+      // PV(np): its P was written and its V slot has landed
+      if (np < nq && ready(&p_full[np & 1], (np >> 1) & 1) &&
+          ready(&vfull[np % kPfVSlots], (np / kPfVSlots) & 1)) {
+        const int m = np, pb = m & 1, vs = m % kPfVSlots;
+        const int nvalid = min(kPfTok, it.tok1 - (it.tok0 + m * kPfTok));
+        if (nvalid < kPfTok) {
+          // V rows past the range may hold anything (NaN included): zero them
+          uint8_t* vb = vring + vs * Cfg::kSlot;
+          const int per = (kPfTok - nvalid) * 8;  // 16-byte chunks per half
+          for (int idx = lane; idx < H2 * per; idx += 32) {
+            const int h = idx / per, rem = idx % per;
+            *reinterpret_cast<uint4*>(vb + h * kHalfK + (nvalid + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int k = 0; k < kPfTok / 16; ++k) {
+            // A = P (rows x tokens, K-major: 64-token halves of 128 B rows)
+            const uint64_t a = smem_desc(p_addr + pb * Cfg::kP + (k >> 2) * kHalfP + (k & 3) * 32, 16, 1024);
+            // B = V (tokens x dims, MN-major: 64-dim halves kHalfK apart)
+            const uint64_t b = smem_desc(v_addr + vs * Cfg::kSlot + k * 2048, kHalfK, 1024);
+            tc_mma(tmem_o + pb * 128, a, b, kIdescPV, ((m >> 1) | k) != 0);
+          }
+          tc_commit(&vempty[vs]);
+          tc_commit(&pv_done[pb]);
+        }
+        __syncwarp();
+        ++np;
+        progressed = true;
+      }
+      if (progressed) {
+        idle_since = clock64();
+      } else if (clock64() - idle_since > kWaitLimitCycles) {
+        ok = false;  // nothing became ready within the wait limit
+      }
     }
-    if (ok && ntiles > 0 && !pv(ntiles - 1)) ok = false;
     if (!ok && lane == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
     if (lane == 0) {
       tc_commit(qk_done);
