@@ -101,6 +101,14 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// L2 policy for data that other CTAs read again soon (prefill K and V, read by
+// every row tile of a sequence).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -6,8 +6,8 @@
 //
 // One CTA per work item (a 128-row tile: the work list uses 128-row tiles
 // for these launches), 128-token key tiles, 12 warps:
-//   warp 0     TMA producer: K and V of each key tile (3-D boxes, 128-byte
-//              swizzle) into 2-slot K and V rings.
+//   warps 0, 2 TMA producers of K and of V: each key tile as 3-D boxes
+//              (128-byte swizzle) into 2-slot K and V rings.
 //   warp 1     allocates TMEM; one thread issues S = Q . K^T (M=128 rows,
 //              N=128 tokens, K-major operands; S double-buffered in TMEM),
 //              then O += P . V for the previous tile (M=128, N=hd; A = P
@@ -21,7 +21,7 @@
 //              O rescaled in TMEM) only when a score exceeds it by more than
 //              2^8. P (fp16) goes to shared memory in the K-major swizzled
 //              layout the PV MMA reads; each group has its own P buffer.
-//   warps 2-3  no role.
+//   warp 3     no role.
 // With the compressed causal mask an item stops after its last query row's
 // position, and only the keys above the diagonal read the mask. Every wait is
 // bounded; on a timeout the CTA records PA_STATUS_BIT_TIMEOUT and exits
@@ -143,18 +143,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
   const uint32_t tmem_s = tmem;        // S buffer b: columns [128 b, 128 b + 128)
   const uint32_t tmem_o = tmem + 256;  // O of group g: columns [256 + 128 g, 256 + 128 g + HD)
 
-  if (warp == 0) {
-    // ================= TMA producer (lane 0) =================
+  if (warp == 0 || warp == 2) {
+    // ================= TMA producers (lane 0): K (warp 0), V (warp 2) =========
+    // Separate producers, so that a K tile never waits behind a V tile whose
+    // slot is still being read.
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
+      const bool is_k = warp == 0;
+      const uint64_t pol = policy_evict_last();  // every row tile of the sequence reads it
       const int32_t* bt_row = P.block_tables + int64_t(it.b) * P.max_blocks_per_seq;
       const int box_rows = bs < kPfTok ? bs : kPfTok;
       const int pieces = kPfTok / box_rows;
-      const int kz = it.kvh * H2;                              // K: 64-dim blocks of this head
-      const int vz = it.kvh * ((P.kv_shared ? P.hk : HD) / 64);  // V (shared: over the K rows)
-      int kiss = 0, viss = 0;
+      // 64-dim blocks of this head in the map's rows (shared KV: V over the K rows)
+      const int z0 = is_k ? it.kvh * H2 : it.kvh * ((P.kv_shared ? P.hk : HD) / 64);
+      const int nslots = is_k ? kPfKSlots : kPfVSlots;
+      uint64_t* fullb = is_k ? kfull : vfull;
+      uint64_t* emptyb = is_k ? kempty : vempty;
+      uint8_t* ring = is_k ? kring : vring;
+      const CUtensorMap* map = is_k ? &tmk : &tmv;
+      int iss = 0;
       bool ok = true;
-      for (int n = 0; n < ntiles && ok; ++n) {
+      for (int n = 0; n < ntiles; ++n) {
         const int t0 = it.tok0 + n * kPfTok;
         int npieces = 0;
         for (int pc = 0; pc < pieces; ++pc) {
@@ -162,48 +170,39 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
           if (tok >= it.tok1) break;
           const int ph = bt_row[tok / bs];
           if (ph < 0 || ph >= P.num_blocks) {
-            set_status(P.status, PA_STATUS_BIT_BLOCK_INDEX);
+            if (is_k) set_status(P.status, PA_STATUS_BIT_BLOCK_INDEX);
             continue;
           }
           ++npieces;
         }
         const uint32_t bytes = uint32_t(npieces) * box_rows * 128 * H2;
-        for (int kv = 0; kv < 2 && ok; ++kv) {
-          const int nslots = kv == 0 ? kPfKSlots : kPfVSlots;
-          int& iss = kv == 0 ? kiss : viss;
-          const int slot = iss % nslots;
-          uint64_t* full = kv == 0 ? &kfull[slot] : &vfull[slot];
-          uint64_t* empty = kv == 0 ? &kempty[slot] : &vempty[slot];
-          if (!mbar_wait(empty, ((iss / nslots) & 1) ^ 1)) {
-            ok = false;
-            break;
-          }
-          uint8_t* dst = (kv == 0 ? kring : vring) + slot * Cfg::kSlot;
-          const CUtensorMap* map = kv == 0 ? &tmk : &tmv;
-          const int z0 = kv == 0 ? kz : vz;
-          if (bytes) mbar_arrive_expect_tx(full, bytes); else mbar_arrive(full);
-          for (int pc = 0; pc < pieces; ++pc) {
-            const int tok = t0 + pc * box_rows;
-            if (tok >= it.tok1) break;
-            const int ph = bt_row[tok / bs];
-            if (ph < 0 || ph >= P.num_blocks) continue;
-            const int row = ph * bs + tok % bs;
-            if (box_rows == kPfTok) {
-              // one box: [H2 halves][128 tokens][128 B] = the slot
-              tma_load_3d(dst, map, full, 0, row, z0, pol);
-            } else {
-              for (int h = 0; h < H2; ++h)
-                tma_load_3d(dst + h * kHalfK + pc * box_rows * 128, map, full, 0, row, z0 + h, pol);
-            }
-          }
-          ++iss;
+        const int slot = iss % nslots;
+        if (!mbar_wait(&emptyb[slot], ((iss / nslots) & 1) ^ 1)) {
+          ok = false;
+          break;
         }
+        uint8_t* dst = ring + slot * Cfg::kSlot;
+        uint64_t* full = &fullb[slot];
+        if (bytes) mbar_arrive_expect_tx(full, bytes); else mbar_arrive(full);
+        for (int pc = 0; pc < pieces; ++pc) {
+          const int tok = t0 + pc * box_rows;
+          if (tok >= it.tok1) break;
+          const int ph = bt_row[tok / bs];
+          if (ph < 0 || ph >= P.num_blocks) continue;
+          const int row = ph * bs + tok % bs;
+          if (box_rows == kPfTok) {
+            // one box: [H2 halves][128 tokens][128 B] = the slot
+            tma_load_3d(dst, map, full, 0, row, z0, pol);
+          } else {
+            for (int h = 0; h < H2; ++h)
+              tma_load_3d(dst + h * kHalfK + pc * box_rows * 128, map, full, 0, row, z0 + h, pol);
+          }
+        }
+        ++iss;
       }
       if (!ok) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
-      for (int i = kiss - kPfKSlots > 0 ? kiss - kPfKSlots : 0; i < kiss; ++i)
-        mbar_wait(&kfull[i % kPfKSlots], (i / kPfKSlots) & 1);
-      for (int i = viss - kPfVSlots > 0 ? viss - kPfVSlots : 0; i < viss; ++i)
-        mbar_wait(&vfull[i % kPfVSlots], (i / kPfVSlots) & 1);
+      for (int i = iss - nslots > 0 ? iss - nslots : 0; i < iss; ++i)
+        mbar_wait(&fullb[i % nslots], (i / nslots) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -312,17 +311,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
       // Q tile: rows r, 64-dim halves, swizzled; 128 threads, 16-byte chunks
       const int st = tid - 128;
       constexpr int kChunks = kPfRows * (HD / 8);
+      constexpr int kPer = kChunks / 128, kRound = kPer < 8 ? kPer : 8;
 #pragma unroll
-      for (int k = 0; k < kChunks / 128; ++k) {
-        const int idx = st + k * 128;
-        const int row = idx / (HD / 8), c = idx % (HD / 8);
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < it.nrows) {
-          const int rq = it.r0 + row;
-          v = *reinterpret_cast<const uint4*>(
-              P.query + (int64_t(it.q_start + rq / G) * P.num_heads + it.kvh * G + rq % G) * HD + c * 8);
+      for (int k0 = 0; k0 < kPer; k0 += kRound) {
+        uint4 v[kRound];  // every load of the round before any store
+#pragma unroll
+        for (int k = 0; k < kRound; ++k) {
+          const int idx = st + (k0 + k) * 128;
+          const int row = idx / (HD / 8), c = idx % (HD / 8);
+          v[k] = make_uint4(0, 0, 0, 0);
+          if (row < it.nrows) {
+            const int rq = it.r0 + row;
+            v[k] = *reinterpret_cast<const uint4*>(
+                P.query + (int64_t(it.q_start + rq / G) * P.num_heads + it.kvh * G + rq % G) * HD + c * 8);
+          }
         }
-        *reinterpret_cast<uint4*>(q_s + (c >> 3) * kHalfQ + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v;
+#pragma unroll
+        for (int k = 0; k < kRound; ++k) {
+          const int idx = st + (k0 + k) * 128;
+          const int row = idx / (HD / 8), c = idx % (HD / 8);
+          *reinterpret_cast<uint4*>(q_s + (c >> 3) * kHalfQ + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v[k];
+        }
       }
       fence_proxy_async();
       __syncwarp();
@@ -347,19 +356,34 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
       if (P.mask_type == PA_MASK_NORM_COMPRESS && __any_sync(0xffffffffu, diag_row)) {
         // a tile reaching above some row's diagonal: read the mask there
         const int mr = min(max(p_row - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
+        const __half* mrow = P.mask + mr * PA_COMPRESS_MASK_SIZE;
 #pragma unroll 1
         for (int cc = 0; cc < kPfTok / 32; ++cc) {
           float x[32];
           tmem_ld32(sbuf + cc * 32, x);
+          // the chunk's mask values, loaded together (indices clamped into the
+          // mask, so every load is in bounds) and used only above the diagonal
+          const bool need = __any_sync(0xffffffffu, diag_row && j0 + cc * 32 + 31 > p_row);
+          __half mv[32];
+          if (need) {
+            const int m0 = j0 + cc * 32 - sigma;  // mask column of this chunk's first key
+            if (m0 >= 0 && m0 + 32 <= PA_COMPRESS_MASK_SIZE && (m0 & 7) == 0) {
+              // 64 contiguous bytes of the row, 16-byte aligned: four vector loads
+              const uint4* src = reinterpret_cast<const uint4*>(mrow + m0);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(mv + 8 * q) = src[q];
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                mv[i] = mrow[min(max(m0 + i, 0), PA_COMPRESS_MASK_SIZE - 1)];
+            }
+          }
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int c = cc * 32 + i, j = j0 + c;
             float v = x[i] * P.scale_log2;
-            if (diag_row && j > p_row && c < jend) {
-              const int mc = min(max(j - sigma, 0), PA_COMPRESS_MASK_SIZE - 1);
-              v += __half2float(P.mask[mr * PA_COMPRESS_MASK_SIZE + mc]) * kLog2e;
-            }
+            if (need && diag_row && j > p_row && c < jend) v += __half2float(mv[i]) * kLog2e;
             v = c < jend ? v : -INFINITY;
             x[i] = v;
             tmax = fmaxf(tmax, v);
