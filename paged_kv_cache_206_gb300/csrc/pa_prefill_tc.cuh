@@ -11,7 +11,7 @@
 //   warp 1     allocates TMEM; one thread issues S = Q . K^T (M=128 rows,
 //              N=128 tokens, K-major operands; S double-buffered in TMEM),
 //              then O += P . V for the previous tile (M=128, N=hd; A = P
-//              K-major, B = V MN-major; O accumulates in TMEM).
+//              from TMEM, B = V MN-major; O accumulates in TMEM).
 //   warps 4-11 softmax in two groups of four that take alternate key tiles,
 //              each with its own running max, sum and O accumulator (merged
 //              per row at the end); one query row per thread (TMEM lane m
@@ -19,8 +19,8 @@
 //              scores come from TMEM in 32-column loads, so max and sum need
 //              no exchange between threads. The reference max is moved (and
 //              O rescaled in TMEM) only when a score exceeds it by more than
-//              2^8. P (fp16) goes to shared memory in the K-major swizzled
-//              layout the PV MMA reads; each group has its own P buffer.
+//              2^8. P (fp16) is written back into the S buffer's TMEM
+//              columns, where the PV MMA takes it as its A operand.
 //   warp 3     no role.
 // With the compressed causal mask an item stops after its last query row's
 // position, and only the keys above the diagonal read the mask. Every wait is
@@ -35,19 +35,36 @@ namespace pa {
 constexpr int kPfTok = 128;      // key tokens per tile (N of S = Q . K^T)
 constexpr int kPfRows = PA_PF_TILE_ROWS;  // query rows per tile (M of both MMAs)
 constexpr int kPfThreads = 384;  // 12 warps
-constexpr int kPfKSlots = 2;
-constexpr int kPfVSlots = 2;
-constexpr int kPfPBufs = 2;
+constexpr int kPfKSlots = 3;
+constexpr int kPfVSlots = 3;
+
+// 16 columns of 32-bit values into this warp's TMEM lane quarter.
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// D (TMEM) += A (TMEM: row m in lane m, K in consecutive 32-bit columns of
+// fp16 pairs) . B (shared memory descriptor).
+__device__ __forceinline__ void tc_mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
 
 template <int HD>
 struct PfCfg {
   static constexpr int kHalves = HD / 64;                       // 64-dim halves of a row
   static constexpr uint32_t kSlot = uint32_t(kPfTok) * HD * 2;  // one K or V tile
   static constexpr uint32_t kQ = uint32_t(kPfRows) * HD * 2;
-  static constexpr uint32_t kP = uint32_t(kPfRows) * kPfTok * 2;
   static constexpr uint32_t q_off = 0;
-  static constexpr uint32_t p_off = q_off + kQ;
-  static constexpr uint32_t k_off = p_off + kPfPBufs * kP;
+  static constexpr uint32_t k_off = q_off + kQ;
   static constexpr uint32_t v_off = k_off + kPfKSlots * kSlot;
   static constexpr uint32_t bars_off = v_off + kPfVSlots * kSlot;
   static constexpr int kBars = 2 * (kPfKSlots + kPfVSlots) + 12;
@@ -70,12 +87,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
   constexpr uint32_t kIdescPV = mma_idesc(kPfRows, HD, 0, 1);
   constexpr uint32_t kHalfK = uint32_t(kPfTok) * 128;  // one 64-dim half of a K/V tile
   constexpr uint32_t kHalfQ = uint32_t(kPfRows) * 128;  // one 64-dim half of Q
-  constexpr uint32_t kHalfP = uint32_t(kPfRows) * 128;  // one 64-token half of P
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint8_t* q_s = smem + Cfg::q_off;
-  uint8_t* p_s = smem + Cfg::p_off;
   uint8_t* kring = smem + Cfg::k_off;
   uint8_t* vring = smem + Cfg::v_off;
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Cfg::bars_off);
@@ -212,7 +227,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
     // ready, so that one group's softmax never holds back the other's next
     // QK. Lane 0 polls; the warp follows its verdicts.
     bool ok = true;
-    const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
+    const uint32_t q_addr = smem_u32(q_s);
     const uint32_t k_addr = smem_u32(kring), v_addr = smem_u32(vring);
     if (ntiles > 0 && !warp_wait(q_ready, 0, lane)) ok = false;
     auto ready = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -223,8 +238,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
     long long idle_since = clock64();
     while (ok && np < ntiles) {
       bool progressed = false;
-      // QK(nq): its K slot has landed and its S buffer was read (tile nq - 2)
-      if (nq < ntiles && (nq < 2 || ready(&s_free[nq & 1], ((nq >> 1) - 1) & 1)) &&
+      // QK(nq): its K slot has landed, and its S buffer's P (tile nq - 2) was
+      // read by PV(nq - 2): issued before this QK by this thread, which the
+      // tensor cores carry out in order
+      if (nq < ntiles && (nq < 2 || (np >= nq - 1 && ready(&s_free[nq & 1], ((nq >> 1) - 1) & 1))) &&
           ready(&kfull[nq % kPfKSlots], (nq / kPfKSlots) & 1)) {
         const int ks = nq % kPfKSlots;
         tc_fence_after();
@@ -266,11 +283,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
         if (lane == 0) {
 #pragma unroll
           for (int k = 0; k < kPfTok / 16; ++k) {
-            // A = P (rows x tokens, K-major: 64-token halves of 128 B rows)
-            const uint64_t a = smem_desc(p_addr + pb * Cfg::kP + (k >> 2) * kHalfP + (k & 3) * 32, 16, 1024);
+            // A = P in TMEM: row m in lane m, 16 tokens = 8 columns of fp16 pairs
             // B = V (tokens x dims, MN-major: 64-dim halves kHalfK apart)
             const uint64_t b = smem_desc(v_addr + vs * Cfg::kSlot + k * 2048, kHalfK, 1024);
-            tc_mma(tmem_o + pb * 128, a, b, kIdescPV, ((m >> 1) | k) != 0);
+            tc_mma_tmem_a(tmem_o + pb * 128, tmem_s + pb * 128 + k * 8, b, kIdescPV, ((m >> 1) | k) != 0);
           }
           tc_commit(&vempty[vs]);
           tc_commit(&pv_done[pb]);
@@ -441,34 +457,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
         break;
       }
       tc_fence_after();
-      // Pass 2: probabilities straight into P (fp16): row r, 16-byte chunks of
-      // 8 tokens, 64-token halves, swizzled. Then the S buffer is free.
+      // Pass 2: probabilities as fp16 pairs into the S buffer's first 64
+      // columns, where the PV MMA reads them: chunk cc's 32 scores (columns
+      // 32cc..) become columns 16cc.., all of which this thread has read.
       float psum = 0.f;
-      uint8_t* pb = p_s + b * Cfg::kP;
 #pragma unroll 1
       for (int cc = 0; cc < kPfTok / 32; ++cc) {
         float x[32];
         tmem_ld32(sbuf + cc * 32, x);
         tmem_wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          float e[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            e[i] = ex2(x[q8 * 8 + i] - m_ref);
-            psum += e[i];
-          }
-          uint4 pk;
-          pk.x = pack_half2(e[0], e[1]);
-          pk.y = pack_half2(e[2], e[3]);
-          pk.z = pack_half2(e[4], e[5]);
-          pk.w = pack_half2(e[6], e[7]);
-          const int c8 = cc * 4 + q8;
-          if (active)
-            *reinterpret_cast<uint4*>(pb + (c8 >> 3) * kHalfP + r * 128 + (((c8 & 7) ^ (r & 7)) << 4)) = pk;
+        for (int i = 0; i < 16; ++i) {
+          const float e0 = ex2(x[2 * i] - m_ref), e1 = ex2(x[2 * i + 1] - m_ref);
+          psum += e0 + e1;
+          pk[i] = pack_half2(e0, e1);
         }
+        tmem_st16u(sbuf + cc * 16, pk);
       }
       l += psum;
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[b]);
@@ -485,7 +493,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
         }
         tmem_wait_st();
       }
-      fence_proxy_async();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[b]);
