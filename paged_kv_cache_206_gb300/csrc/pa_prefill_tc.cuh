@@ -7,11 +7,11 @@
 // One CTA per work item (a 128-row tile: the work list uses 128-row tiles
 // for these launches), 128-token key tiles, 12 warps:
 //   warps 0, 2 TMA producers of K and of V: each key tile as 3-D boxes
-//              (128-byte swizzle) into 2-slot K and V rings.
+//              (128-byte swizzle) into 3-slot K and V rings.
 //   warp 1     allocates TMEM; one thread issues S = Q . K^T (M=128 rows,
-//              N=128 tokens, K-major operands; S double-buffered in TMEM),
-//              then O += P . V for the previous tile (M=128, N=hd; A = P
-//              from TMEM, B = V MN-major; O accumulates in TMEM).
+//              N=128 tokens, K-major operands; S double-buffered in TMEM)
+//              and O += P . V (M=128, N=hd; A = P from TMEM, B = V MN-major;
+//              O accumulates in TMEM), each as soon as its inputs are ready.
 //   warps 4-11 softmax in two groups of four that take alternate key tiles,
 //              each with its own running max, sum and O accumulator (merged
 //              per row at the end); one query row per thread (TMEM lane m
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
   uint64_t* vfull = kempty + kPfKSlots;
   uint64_t* vempty = vfull + kPfVSlots;
   uint64_t* s_full = vempty + kPfVSlots;  // [2] S buffer written
-  uint64_t* s_free = s_full + 2;          // [2] S buffer read by the softmax warps
+  uint64_t* s_free = s_full + 2;          // [2] S buffer read and P written by the softmax warps
   uint64_t* p_full = s_full + 4;          // [2] P buffer written
   uint64_t* pv_done = s_full + 6;         // [2] PV that read P buffer b complete
   uint64_t* qk_done = s_full + 8;
