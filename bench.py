@@ -227,6 +227,21 @@ def cpu_baseline(w, max_seconds=20.0):
                       f"OpenMP over (sequence, kv head)"}
 
 
+def reduce_over_ranks(maxes, sums, world, device):
+    """Whole-job figures of independent replicas: the slowest rank's times
+    (max) and the bytes and tokens of all ranks (sum). One collective each; the
+    data path itself has none."""
+    if world <= 1:
+        return list(maxes), list(sums)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(maxes), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor(list(sums), device=device, dtype=torch.float64)
+    dist.all_reduce(u)
+    return t.tolist(), u.tolist()
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -369,15 +384,8 @@ def main():
     ms = statistics.mean(times)
     dec_ms = statistics.mean(dec_times)
     e2e_s = statistics.mean(e2e_t) if e2e_t else float("nan")
-    if world > 1:
-        t = torch.tensor([ms, dec_ms, e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, dec_ms, e2e_s = t.tolist()
-        tot = torch.tensor([kv_bytes, qo_bytes, w.total_q], device=dev, dtype=torch.float64)
-        dist.all_reduce(tot)
-        kv_all, qo_all, q_all = tot.tolist()
-    else:
-        kv_all, qo_all, q_all = kv_bytes, qo_bytes, w.total_q
+    (ms, dec_ms, e2e_s), (kv_all, qo_all, q_all) = reduce_over_ranks(
+        [ms, dec_ms, e2e_s], [kv_bytes, qo_bytes, w.total_q], world, dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
