@@ -3,9 +3,11 @@
 One step is one pass of the whole device path over one synthetic batch: the
 attention kernel over the planned work list plus the split-KV combine. The
 work list comes from pa_plan before the timed region (it is host code, timed
-separately as plan_us); the end-to-end number (`e2e`) puts the plan, the
-host->device copies of the step's inputs and the device->host read of the
-output inside its timed region.
+separately as plan_us). The end-to-end number (`e2e`) starts from pinned host
+buffers: each timed step replays one recorded CUDA graph that copies the
+step's inputs to the device, plans on the device, runs attention and combine
+and copies the output back, and the host waits for it. The same step planned
+on the host with direct launches is reported beside it (`e2e.host_planned`).
 
 Default workload: GQA decode, B=64, H=32, Hk=8, hk=hv=128, block_size=128,
 context lengths uniform in [1, 4096], one query token per sequence, seed 0.
@@ -347,45 +349,56 @@ def main():
     # the dominant kernel alone: the same launch without the combine pass
     dec_times = time_device(decode_only, max(50, args.steps // 4), 5, flush, stream)
 
-    # end to end through the C ABI with host buffers: the step's inputs sit in
-    # one pinned host arena (query, block tables, lengths; the planner writes
-    # the work and combine lists into it), one copy moves it to the device, the
-    # output comes back into pinned memory, and the host waits for it
-    hs = pa.HostStep(db.cfg, db.key_cache, db.value_cache, w.total_q, mask=db.mask,
-                     alibi_slopes=db.alibi_slopes)
-    hs.query.copy_(torch.from_numpy(np.ascontiguousarray(w.query)))
-    hs.block_tables.copy_(torch.from_numpy(np.ascontiguousarray(w.block_tables)))
-    hs.context_lens.copy_(torch.from_numpy(np.ascontiguousarray(w.context_lens)))
-    if hs.q_seqlens is not None:
-        hs.q_seqlens.copy_(torch.from_numpy(np.ascontiguousarray(w.q_seqlens)))
+    # end to end through the C ABI with host buffers. The step's inputs sit in
+    # one pinned host arena (query, block tables, lengths). GraphStep replays
+    # one recorded graph per step: the arena's copy to the device, the device
+    # planner, attention, combine and the output's copy back into pinned
+    # memory; the host waits for it. HostStep, timed beside it, plans on the
+    # host and launches each call directly.
+    def fill(st):
+        st.query.copy_(torch.from_numpy(np.ascontiguousarray(w.query)))
+        st.block_tables.copy_(torch.from_numpy(np.ascontiguousarray(w.block_tables)))
+        st.context_lens.copy_(torch.from_numpy(np.ascontiguousarray(w.context_lens)))
+        if st.q_seqlens is not None:
+            st.q_seqlens.copy_(torch.from_numpy(np.ascontiguousarray(w.q_seqlens)))
+        return st
 
-    def e2e_step():
-        hs.run(stream)
+    gs = fill(pa.GraphStep(db.cfg, db.key_cache, db.value_cache, w.total_q, mask=db.mask,
+                           alibi_slopes=db.alibi_slopes))
+    hs = fill(pa.HostStep(db.cfg, db.key_cache, db.value_cache, w.total_q, mask=db.mask,
+                          alibi_slopes=db.alibi_slopes))
 
-    for _ in range(min(5, args.e2e_steps)):
-        e2e_step()
-    e2e_t = []
-    for _ in range(args.e2e_steps):
-        flush_l2(flush)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        e2e_step()
-        e2e_t.append(time.perf_counter() - t0)
-    h2d = hs.last_h2d_bytes
-    d2h = hs.out.numel() * hs.out.element_size()
+    def time_host(fn):
+        for _ in range(min(5, args.e2e_steps)):
+            fn()
+        out = []
+        for _ in range(args.e2e_steps):
+            flush_l2(flush)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            out.append(time.perf_counter() - t0)
+        return out
+
+    e2e_t = time_host(gs.run)
+    host_t = time_host(lambda: hs.run(stream))
+    h2d = gs.h2d_bytes
+    d2h = gs.out.numel() * gs.out.element_size()
     if e2e_t:
-        st, bits = hs.status(stream)
-        if st != pa.PA_OK:
-            raise RuntimeError(f"e2e kernel status {pa.status_string(st)} ({bits})")
+        for name, s_ in (("graph", gs.status()), ("host-planned", hs.status(stream))):
+            if s_[0] != pa.PA_OK:
+                raise RuntimeError(f"e2e {name} status {pa.status_string(s_[0])} ({s_[1]})")
         db.forward(stream)
-        if not torch.equal(hs.out, db.out.cpu()):
+        ref_out = db.out.cpu()
+        if not (torch.equal(gs.out, ref_out) and torch.equal(hs.out, ref_out)):
             raise RuntimeError("end-to-end output differs from the device-resident run")
 
     ms = statistics.mean(times)
     dec_ms = statistics.mean(dec_times)
     e2e_s = statistics.mean(e2e_t) if e2e_t else float("nan")
-    (ms, dec_ms, e2e_s), (kv_all, qo_all, q_all) = reduce_over_ranks(
-        [ms, dec_ms, e2e_s], [kv_bytes, qo_bytes, w.total_q], world, dev)
+    host_s = statistics.mean(host_t) if host_t else float("nan")
+    (ms, dec_ms, e2e_s, host_s), (kv_all, qo_all, q_all) = reduce_over_ranks(
+        [ms, dec_ms, e2e_s, host_s], [kv_bytes, qo_bytes, w.total_q], world, dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -436,7 +449,12 @@ def main():
                          kernel_ms=dec_ms),
         "e2e": None if not e2e_t else {
             "value": kv_all / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3},
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3,
+            "path": "GraphStep: one graph replay per step (copy in, device plan, attention, "
+                    "combine, copy out), host waits",
+            "host_planned": {"value": kv_all / host_s / 1e9, "ms_per_step": host_s * 1e3,
+                             "h2d_bytes_per_step": int(hs.last_h2d_bytes),
+                             "path": "HostStep: pa_plan on the host, direct launches"}},
         "gpu_launches": args.steps * (1 + (1 if n_comb else 0)),
         "clocks": clk.summary(),
         "cpu_baseline": base,

@@ -448,3 +448,106 @@ class DevicePlanStep:
 
     def status(self, stream=None):
         return pa_status_read(self.workspace, stream)
+
+
+class GraphStep:
+    """One attention step recorded once as a CUDA graph and replayed per step.
+
+    The step's inputs live in one pinned host arena (views ``query``,
+    ``block_tables``, ``context_lens``, ``q_seqlens``). The graph holds: one
+    host-to-device copy of the arena, the device planner (pa_plan_device), the
+    forward pass over its lists (pa_forward_device_plan) and the copy of the
+    output back into the pinned ``out`` tensor. :meth:`run` replays it and
+    waits, so a decode loop costs one graph launch per step. The launches do
+    not depend on the lengths (grids are pa_plan_bounds' capacities), which is
+    what allows the recording.
+    """
+
+    def __init__(self, cfg: pa_config, key_cache, value_cache, total_q: int, mask=None,
+                 alibi_slopes=None):
+        import torch
+        self.cfg = cfg
+        dev = key_cache.device
+        self.key_cache, self.value_cache = key_cache, value_cache
+        self.mask, self.alibi_slopes = mask, alibi_slopes
+        B, H, hk, hv = cfg.batch, cfg.num_heads, cfg.head_size_k, cfg.head_size_v
+        has_ql = cfg.max_seqlen_q > 1
+        self.total_q = int(total_q)
+        sizes = [("query", self.total_q * H * hk * 2),
+                 ("block_tables", B * cfg.max_blocks_per_seq * 4),
+                 ("context_lens", B * 4), ("q_seqlens", B * 4 if has_ql else 0)]
+        self.offsets, off = {}, 0
+        for name, n in sizes:
+            self.offsets[name] = off
+            off = _align(off + n)
+        self.arena_bytes = off
+        self.h_arena = torch.zeros(off, dtype=torch.uint8).pin_memory()
+        self.d_arena = torch.zeros(off, dtype=torch.uint8, device=dev)
+
+        def view(t, name, dtype, shape):
+            o = self.offsets[name]
+            n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            return t[o:o + n].view(dtype).view(shape)
+
+        self.query = view(self.h_arena, "query", torch.float16, (self.total_q, H, hk))
+        self.block_tables = view(self.h_arena, "block_tables", torch.int32, (B, cfg.max_blocks_per_seq))
+        self.context_lens = view(self.h_arena, "context_lens", torch.int32, (B,))
+        self.q_seqlens = view(self.h_arena, "q_seqlens", torch.int32, (B,)) if has_ql else None
+        self._dq = view(self.d_arena, "query", torch.float16, (self.total_q, H, hk))
+        self._dbt = view(self.d_arena, "block_tables", torch.int32, (B, cfg.max_blocks_per_seq))
+        self._dcl = view(self.d_arena, "context_lens", torch.int32, (B,))
+        self._dql = view(self.d_arena, "q_seqlens", torch.int32, (B,)) if has_ql else None
+        self.work_cap, self.comb_cap, ws = pa_plan_bounds(cfg)
+        self.work = torch.zeros((self.work_cap, PA_WORK_INTS), dtype=torch.int32, device=dev)
+        self.combine = torch.zeros((max(self.comb_cap, 1), PA_COMBINE_INTS), dtype=torch.int32,
+                                   device=dev)
+        self.counts = torch.zeros(PA_PLAN_COUNTS, dtype=torch.int32, device=dev)
+        self.workspace = torch.zeros(max(ws, PA_STATUS_BYTES), dtype=torch.uint8, device=dev)
+        self.d_out = torch.empty((self.total_q, H, hv), dtype=torch.float16, device=dev)
+        self.out = torch.empty((self.total_q, H, hv), dtype=torch.float16).pin_memory()
+        self.h2d_bytes = self.arena_bytes
+        self.stream = torch.cuda.Stream(device=dev)
+        self.graph = None
+
+    def _enqueue(self):
+        import torch
+        lib, cfg, s = load_library(), self.cfg, self.stream
+        with torch.cuda.stream(s):
+            self.d_arena.copy_(self.h_arena, non_blocking=True)
+        _check(lib.pa_plan_device(
+            ctypes.byref(cfg), _tptr(self._dcl), _tptr(self._dql), _tptr(self.work),
+            self.work_cap, _tptr(self.combine), self.comb_cap, _tptr(self.counts),
+            _tptr(self.workspace), ctypes.c_void_p(s.cuda_stream)), "pa_plan_device")
+        _check(lib.pa_forward_device_plan(
+            ctypes.byref(cfg), _tptr(self._dq), _tptr(self.key_cache), _tptr(self.value_cache),
+            _tptr(self._dbt), _tptr(self._dcl), _tptr(self._dql), _tptr(self.mask),
+            _tptr(self.alibi_slopes), _tptr(self.work), self.work_cap, _tptr(self.combine),
+            self.comb_cap, _tptr(self.counts), _tptr(self.workspace), self.workspace.numel(),
+            _tptr(self.d_out), ctypes.c_void_p(s.cuda_stream)), "pa_forward_device_plan")
+        with torch.cuda.stream(s):
+            self.out.copy_(self.d_out, non_blocking=True)
+
+    def record(self):
+        """Run the step once directly (kernel attributes and tensor maps are set
+        up then), then record it as a graph."""
+        import torch
+        self._enqueue()
+        self.stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            self._enqueue()
+        self.graph = g
+
+    def run(self):
+        """Replay the step and wait for it; returns the pinned ``out`` tensor."""
+        import torch
+        if self.graph is None:
+            self.record()
+        # replay() launches on the current stream: make that the step's own
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()
+        self.stream.synchronize()
+        return self.out
+
+    def status(self):
+        return pa_status_read(self.workspace, self.stream)

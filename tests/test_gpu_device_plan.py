@@ -154,3 +154,35 @@ def test_graph_replay_with_changing_lengths(oracle_mod, name):
         err = np.abs(got - ref)
         assert np.isfinite(got).all()
         assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (cut, err.max(), err.mean())
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_graph_step_host_buffers(oracle_mod, name):
+    """GraphStep: inputs written into pinned host views, one graph replay per
+    step (copy in, device plan, attention, combine, copy out). New lengths and
+    a new query between replays must give the oracle's answer for each."""
+    w = CASES[name]()
+    db = pa.DeviceBatch(w)
+    gs = pa.GraphStep(db.cfg, db.key_cache, db.value_cache, w.total_q, mask=db.mask,
+                      alibi_slopes=db.alibi_slopes)
+    gs.block_tables.copy_(torch.from_numpy(np.ascontiguousarray(w.block_tables)))
+    if gs.q_seqlens is not None:
+        gs.q_seqlens.copy_(torch.from_numpy(np.ascontiguousarray(w.q_seqlens)))
+    rng = np.random.default_rng(90)
+    q = w.q_seqlens
+    for step, cut in enumerate((0, 150, 600)):
+        lens = np.maximum(w.context_lens - cut, q).astype(np.int32)
+        query = w.query if step == 0 else (
+            rng.standard_normal(w.query.shape) * 0.5).astype(np.float16)
+        wi = dataclasses.replace(w, context_lens=lens, query=query)
+        gs.context_lens.copy_(torch.from_numpy(lens))
+        gs.query.copy_(torch.from_numpy(np.ascontiguousarray(query)))
+        gs.out.fill_(float("nan"))
+        got = gs.run().double().numpy()
+        st, bits = gs.status()
+        assert st == pa.PA_OK, (st, bits)
+        ref, _ = oracle_mod.attention(wi, threads=CORES)
+        err = np.abs(got - ref)
+        assert np.isfinite(got).all()
+        assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (cut, err.max(), err.mean())
+    assert gs.graph is not None
