@@ -205,6 +205,13 @@ def time_device(fn, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def percentiles(xs):
+    """median, p10 and p90 of a list (nearest rank)."""
+    ys = sorted(xs)
+    pick = lambda f: ys[min(len(ys) - 1, max(0, int(round(f * (len(ys) - 1)))))]
+    return {"median": pick(0.5), "p10": pick(0.1), "p90": pick(0.9)}
+
+
 def cpu_baseline(w, max_seconds=20.0):
     """The oracle on this machine's cores, on the whole batch or a prefix of it
     sized to stay within about max_seconds."""
@@ -394,6 +401,7 @@ def main():
             raise RuntimeError("end-to-end output differs from the device-resident run")
 
     ms = statistics.mean(times)
+    step_pct = percentiles(times)
     dec_ms = statistics.mean(dec_times)
     e2e_s = statistics.mean(e2e_t) if e2e_t else float("nan")
     host_s = statistics.mean(host_t) if host_t else float("nan")
@@ -443,6 +451,7 @@ def main():
             "l2": "flushed before every step, outside the events: 512 MB written, then 256 MB read back",
             "plan_us": plan_us, "parallelism": f"replica x{world}" if world > 1 else "single",
         },
+        "step_ms": dict(step_pct, mean=ms),
         "query_tokens_per_s": q_all / (ms * 1e-3),
         "pct_of_nominal_8tbs": 100.0 * value / NOMINAL_HBM_GBS,
         "roofline": dict(roof, traffic=traffic, peak_kind=peak_kind, kernel=kernel,

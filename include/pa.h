@@ -153,12 +153,19 @@ typedef struct pa_config {
  *   c_bal = ceil(W / (k * num_sms))
  *   RT    = min(TR, G * max_seqlen_q)   (rows a full tile really holds)
  *   c_min = ceil(64 * RT * hv / (bs * (hk + hv)))
- *   c     = max(1, c_bal, c_min)
+ *   c0    = max(1, c_bal, c_min)
+ * and c = c0 when TR <= PA_FMA_MAX_ROWS. For wider tiles (tcgen05 kernels, one
+ * CTA per SM, so items run in waves of num_sms) the wave fit follows:
+ *   items(x) = sum_b Hk * QT_b * ceil(NB_b / x)
+ *   c = the x in [c0, min(2 * c0, c0 + 31, max(c0, max_b NB_b))] with the
+ *       least ceil(items(x) / num_sms) * x, the smallest such x on a tie
  * (c_bal aims at about k work items per SM so that variable lengths
  * balance: eight for the CUDA-core and mma.sync kernels, of which several CTAs
  * share an SM, two for the tcgen05 kernel, which holds an SM alone and pays a
  * longer fixed cost per item; c_min keeps the partial results that a split
- * writes and re-reads below about a sixteenth of the KV bytes of the split.)
+ * writes and re-reads below about a sixteenth of the KV bytes of the split;
+ * the wave fit lengthens the chunk a little when that saves a nearly empty
+ * last wave of items, waves x chunk standing for the launch's time.)
  * Sequence b has S_b = ceil(NB_b / c) splits; split s covers KV blocks
  * [s * c, min(NB_b, (s + 1) * c)).
  *
@@ -291,8 +298,10 @@ pa_status pa_forward_noalloc(const pa_config* cfg, const void* query, const void
  *   configuration admits, and a workspace size that holds their partial
  *   rows. With tiles T = batch * Hk * ceil(G * max_seqlen_q / TR):
  *   comb_cap = T; work_cap = T * ceil(max_blocks_per_seq / chunk_blocks) for
- *   an explicit chunk, else 8 * num_sms + T (the automatic chunk is at least
- *   W / (8 * num_sms)); workspace for work_cap * TR partial rows.
+ *   an explicit chunk, else 8 * num_sms + T (the automatic chunk, the wave
+ *   fit included, is at least W / (8 * num_sms)); workspace for
+ *   work_cap * TR partial rows. Fails with PA_ERR_INVALID_ARG when the
+ *   automatic chunk is asked for with num_sms <= 0, as pa_plan_device does.
  */
 pa_status pa_plan_bounds(const pa_config* cfg, int64_t* work_cap, int64_t* comb_cap,
                          size_t* workspace_bytes);

@@ -201,7 +201,10 @@ static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
  *                  max(1, ceil(sum_b NB_b*Hk*QT_b / (k*num_sms)),
  *                         ceil(64*RT*hv / (bs*(hk+hv))))
  *                  with RT = min(TR, G * maxq), the rows a full tile holds,
- *                  and k = 8 when TR <= 8, else 2
+ *                  and k = 8 when TR <= 8, else 2; then, when TR > 8 (one CTA
+ *                  per SM), the wave fit: of c0 = that value and the chunks
+ *                  up to min(2*c0, c0 + 31, max(c0, max_b NB_b)), the one with
+ *                  the least ceil(items(c) / num_sms) * c, the first on a tie
  *   splits         S_b = ceil(NB_b / c); split s = blocks [s*c, min(NB_b, (s+1)*c))
  *   items          (b, kvh, qt, s) lexicographic; 8 ints
  *                  {b, kvh, row_begin, row_end, kb_begin, kb_end, q_start, slot}
@@ -235,6 +238,30 @@ int oracle_plan(int batch, int num_heads, int kv_heads, int hk, int hv, int bloc
     c = 1;
     if (c_bal > c) c = c_bal;
     if (c_min > c) c = c_min;
+    if (TR > 8) {
+      int64_t max_nb = 0;
+      for (int b = 0; b < batch; ++b) {
+        const int64_t nb = cdiv(context_lens[b], block_size);
+        if (nb > max_nb) max_nb = nb;
+      }
+      int64_t last = 2 * c;
+      if (c + 31 < last) last = c + 31;
+      if ((max_nb > c ? max_nb : c) < last) last = max_nb > c ? max_nb : c;
+      int64_t best = c, best_cost = -1;
+      for (int64_t cand = c; cand <= last; ++cand) {
+        int64_t n = 0;
+        for (int b = 0; b < batch; ++b) {
+          const int64_t q = q_seqlens ? q_seqlens[b] : 1;
+          n += kv_heads * cdiv(G * q, TR) * cdiv(cdiv(context_lens[b], block_size), cand);
+        }
+        const int64_t cost = cdiv(n, (int64_t)num_sms) * cand;
+        if (best_cost < 0 || cost < best_cost) {
+          best_cost = cost;
+          best = cand;
+        }
+      }
+      c = best;
+    }
   }
   /* first pass: counts */
   int64_t items = 0, combines = 0, prow = 0;

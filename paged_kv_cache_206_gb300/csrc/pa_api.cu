@@ -310,6 +310,7 @@ extern "C" pa_status pa_plan_bounds(const pa_config* cfg, int64_t* work_cap, int
   const pa_status st = validate_config(cfg);
   if (st != PA_OK) return st;
   const pa_config& c = *cfg;
+  if (c.chunk_blocks < 0 || (c.chunk_blocks == 0 && c.num_sms <= 0)) return PA_ERR_INVALID_ARG;
   const int64_t TR = tile_rows(c);
   const int64_t rows = int64_t(c.num_heads / c.kv_heads) * max_q(c);
   const int64_t tiles = int64_t(c.batch) * c.kv_heads * cdiv(rows, TR);
@@ -332,6 +333,7 @@ extern "C" pa_status pa_plan_device(const pa_config* cfg, const int32_t* context
   const pa_config& c = *cfg;
   if (!context_lens || !work || !counts || !workspace || (comb_cap > 0 && !combine))
     return PA_ERR_INVALID_ARG;
+  if (c.chunk_blocks < 0 || (c.chunk_blocks == 0 && c.num_sms <= 0)) return PA_ERR_INVALID_ARG;
   if (work_cap < 1 || comb_cap < 0 || work_cap > INT32_MAX || comb_cap > INT32_MAX)
     return PA_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return PA_ERR_INVALID_ARG;

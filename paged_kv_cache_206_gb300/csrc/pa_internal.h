@@ -27,6 +27,22 @@ inline int64_t tile_rows(const pa_config& c) {
   return (r > PA_TC_TILE_ROWS && pf_heads) ? PA_PF_TILE_ROWS : PA_TC_TILE_ROWS;
 }
 
+#ifdef __CUDACC__
+#define PA_HOST_DEVICE __host__ __device__
+#else
+#define PA_HOST_DEVICE
+#endif
+
+// Last chunk the wave fit of the automatic chunk rule tries after the
+// balance chunk c0: at most twice c0, at most 31 past it, and none past the
+// longest sequence's block count (from there on every chunk gives the same
+// items, so a longer one only costs).
+PA_HOST_DEVICE inline int64_t wave_fit_hi(int64_t c0, int64_t max_nb) {
+  int64_t hi = 2 * c0 < c0 + 31 ? 2 * c0 : c0 + 31;
+  const int64_t cap = max_nb > c0 ? max_nb : c0;
+  return hi < cap ? hi : cap;
+}
+
 struct WorkspaceLayout {
   size_t partial_o;    // byte offset of the fp32 [P, hv] partial outputs
   size_t partial_lse;  // byte offset of the fp32 [P] log-sum-exps

@@ -68,7 +68,7 @@ extern "C" pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens,
   const int64_t TR = pa::tile_rows(c), maxq = pa::max_q(c);
 
   // Per-sequence checks, and the work measure of the automatic chunk rule.
-  int64_t W = 0, total_q = 0;
+  int64_t W = 0, total_q = 0, maxNB = 0;
   for (int b = 0; b < c.batch; ++b) {
     const int64_t L = context_lens[b];
     const int64_t q = q_seqlens ? q_seqlens[b] : 1;
@@ -79,6 +79,7 @@ extern "C" pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens,
     if (NB > c.max_blocks_per_seq) return PA_ERR_INVALID_ARG;
     W += NB * Hk * cdiv(G * q, TR);
     total_q += q;
+    maxNB = std::max(maxNB, NB);
   }
   if (total_q * c.num_heads > INT32_MAX) return PA_ERR_INVALID_ARG;
 
@@ -93,6 +94,26 @@ extern "C" pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens,
     const int64_t RT = std::min(TR, G * maxq);  // rows a full tile really holds
     const int64_t lo = cdiv(64 * RT * c.head_size_v, bs * (c.head_size_k + c.head_size_v));
     chunk = std::max<int64_t>(1, std::max(bal, lo));
+    if (TR > PA_FMA_MAX_ROWS) {
+      // One CTA per SM: items run in waves of num_sms. Of the chunks
+      // chunk .. wave_fit_hi(chunk, maxNB), take the one with the least
+      // waves x chunk (the first on a tie).
+      const int64_t hi = pa::wave_fit_hi(chunk, maxNB);
+      int64_t best = chunk, best_cost = -1;
+      for (int64_t cc = chunk; cc <= hi; ++cc) {
+        int64_t n = 0;
+        for (int b = 0; b < c.batch; ++b) {
+          const int64_t q = q_seqlens ? q_seqlens[b] : 1;
+          n += Hk * cdiv(G * q, TR) * cdiv(cdiv(context_lens[b], bs), cc);
+        }
+        const int64_t cost = cdiv(n, int64_t(c.num_sms)) * cc;
+        if (best_cost < 0 || cost < best_cost) {
+          best_cost = cost;
+          best = cc;
+        }
+      }
+      chunk = best;
+    }
   }
 
   // Counts.

@@ -54,14 +54,19 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanPara
   __shared__ int32_t off_pr[PA_MAX_BATCH + 1];  // partial rows before b
   __shared__ int32_t off_q[PA_MAX_BATCH + 1];   // query tokens before b
   __shared__ int64_t red[kPlanThreads / 32];
-  __shared__ int err, chunk_s;
+  __shared__ int err, chunk_s, max_nb_s;
+  __shared__ int64_t cost_s[kPlanThreads / 32];
   const int tid = threadIdx.x;
   const int B = D.batch, Hk = D.kv_heads, G = D.group, bs = D.block_size, TR = D.tr;
-  if (tid == 0) err = 0;
+  if (tid == 0) {
+    err = 0;
+    max_nb_s = 0;
+  }
   __syncthreads();
 
   // pass 0: checks and the work measure of the automatic chunk rule
   int64_t w = 0;
+  int mnb = 0;
   for (int b = tid; b < B; b += kPlanThreads) {
     const int64_t L = D.context_lens[b];
     const int64_t q = D.q_seqlens ? D.q_seqlens[b] : 1;
@@ -71,7 +76,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanPara
       continue;
     }
     w += NB * Hk * dcdiv(G * q, TR);
+    mnb = NB > mnb ? int(NB) : mnb;
   }
+  atomicMax(&max_nb_s, mnb);
   const int64_t W = block_sum64(w, red);
   if (tid == 0) {
     int64_t c = D.chunk_blocks;
@@ -85,6 +92,37 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanPara
     chunk_s = int(c < INT32_MAX ? c : INT32_MAX);
   }
   __syncthreads();
+  if (D.chunk_blocks <= 0 && TR > PA_FMA_MAX_ROWS) {
+    // wave fit (one CTA per SM): warp j prices the chunk c0 + j as its
+    // waves x chunk; thread 0 takes the least, the first on a tie
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t c0 = chunk_s, cc = c0 + warp;
+    const bool cand = cc <= wave_fit_hi(c0, max_nb_s);
+    int64_t n = 0;
+    if (cand) {
+      for (int b = lane; b < B; b += 32) {
+        const int64_t L = D.context_lens[b];
+        const int64_t q = D.q_seqlens ? D.q_seqlens[b] : 1;
+        if (q < 1 || L < q) continue;  // reported through err
+        n += int64_t(Hk) * dcdiv(int64_t(G) * q, TR) * dcdiv(dcdiv(L, bs), cc);
+      }
+    }
+    for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    if (lane == 0) cost_s[warp] = cand ? dcdiv(n, int64_t(D.num_sms)) * cc : -1;
+    __syncthreads();
+    if (tid == 0) {
+      int64_t best = c0, best_cost = -1;
+      for (int j = 0; j < kPlanThreads / 32; ++j) {
+        if (cost_s[j] < 0) continue;
+        if (best_cost < 0 || cost_s[j] < best_cost) {
+          best_cost = cost_s[j];
+          best = c0 + j;
+        }
+      }
+      chunk_s = int(best < INT32_MAX ? best : INT32_MAX);
+    }
+    __syncthreads();
+  }
   const int64_t c = chunk_s;
 
   // pass 1: per-sequence counts (64-bit totals checked against int32)

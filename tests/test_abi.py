@@ -128,6 +128,13 @@ def test_plan_bounds_and_device_plan_host_checks(lib):
     assert dev(c, ws=ctypes.c_void_p((1 << 20) + 64)) == pa.PA_ERR_INVALID_ARG
     assert dev(_cfg(block_size=8)) == pa.PA_ERR_INVALID_ARG
     assert dev(_cfg(mask_type=4)) == pa.PA_ERR_UNSUPPORTED
+    # the automatic chunk rule needs the SM count (the device planner divides by it)
+    assert dev(_cfg(chunk_blocks=0, num_sms=0)) == pa.PA_ERR_INVALID_ARG
+    assert dev(_cfg(chunk_blocks=-1)) == pa.PA_ERR_INVALID_ARG
+    w_, c_, s_ = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_size_t()
+    for bad in (_cfg(chunk_blocks=0, num_sms=0), _cfg(chunk_blocks=-1)):
+        assert lib.pa_plan_bounds(ctypes.byref(bad), ctypes.byref(w_), ctypes.byref(c_),
+                                  ctypes.byref(s_)) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_forward_device_plan(ctypes.byref(c), fake, fake, fake, fake, fake, None, None,
                                       None, fake, 4, None, 0, None, fake, 256, fake,
                                       None) == pa.PA_ERR_INVALID_ARG  # counts required

@@ -76,7 +76,7 @@ def random_case(seed):
                          block_size=bs if hk <= 256 else min(bs, 128), num_blocks=10 ** 6,
                          max_blocks_per_seq=int(-(-ctx.max() // bs)) + int(rng.integers(0, 3)),
                          max_seqlen_q=maxq, chunk_blocks=chunk,
-                         num_sms=int(rng.choice([1, 148, 152])))
+                         num_sms=int(rng.choice([1, 4, 16, 148, 152])))
     return cfg, ctx, ql
 
 
@@ -96,6 +96,29 @@ def test_device_plan_equals_host_plan(seed):
                                       int(counts[2]) * 4)
     # nothing past the counts was written
     assert (work[n:] == -7).all() and (comb[m:] == -7).all()
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_device_wave_fit_equals_host(seed):
+    """Wide tiles (one CTA per SM) with the automatic chunk: the device
+    planner's wave fit (one warp per candidate chunk) picks the host's chunk."""
+    rng = np.random.default_rng(900 + seed)
+    G = int(rng.choice([16, 64]))
+    hk = int(rng.choice([128, 576]))
+    hv = 512 if hk == 576 else hk
+    bs = int(rng.choice([16, 64]))
+    B = int(rng.choice([6, 64, 300]))
+    ctx = rng.integers(1, 9000, size=B).astype(np.int32)
+    cfg = pa.make_config(batch=B, num_heads=G, kv_heads=1, head_size_k=hk, head_size_v=hv,
+                         block_size=bs, num_blocks=10 ** 6,
+                         max_blocks_per_seq=int(-(-ctx.max() // bs)), chunk_blocks=0,
+                         num_sms=int(rng.choice([3, 16, 152])))
+    host = pa.pa_plan(cfg, ctx, None)
+    counts, work, comb, (st, bits) = device_lists(cfg, ctx, None)
+    assert st == pa.PA_OK and bits == 0
+    n, m = host.work.shape[0], host.combine.shape[0]
+    assert counts.tolist()[:2] == [n, m]
+    assert np.array_equal(work[:n], host.work) and np.array_equal(comb[:m], host.combine)
 
 
 def test_device_plan_reports_bad_lengths_and_small_capacity():

@@ -125,6 +125,73 @@ def test_auto_chunk_rule_values(lib):
     assert set((p.work[:, 5] - p.work[:, 4]).tolist()) == {8}
 
 
+def test_auto_chunk_wave_fit(lib, oracle_mod):
+    """Row tiles above 8 rows run one CTA per SM, so the automatic chunk is
+    then refined: of c0 .. min(2 c0, c0 + 31, max(c0, max NB)) the chunk with
+    the least ceil(items / num_sms) * chunk is taken, the first on a tie."""
+    # 16 heads on one kv head (TR = 64, 16 real rows), hk = hv = 128, bs = 128,
+    # 4 SMs: c_min = ceil(64*16*128 / (128*256)) = 4.
+    base = dict(num_heads=16, kv_heads=1, head_size_k=128, block_size=128, num_sms=4,
+                max_blocks_per_seq=20)
+    # six sequences of 20 blocks: c_bal = ceil(120 / 8) = 15 gives 12 items in
+    # 3 waves (cost 45); chunks 16-19 keep 12 items (48..57); 20 gives 6 items
+    # in 2 waves (cost 40), and the search stops at max NB = 20
+    c = cfg(batch=6, **base)
+    ctx = np.full(6, 20 * 128, np.int32)
+    p = pa.pa_plan(c, ctx)
+    assert p.work.shape[0] == 6 and p.combine.shape[0] == 0
+    assert set((p.work[:, 5] - p.work[:, 4]).tolist()) == {20}
+    # one sequence of 9 blocks: W = 109, c_bal = 14: 11 items, 3 waves (42);
+    # 15..19: 11 items (45..57); 20: 6 items, 2 waves (40)
+    ctx = np.array([20 * 128] * 5 + [9 * 128], np.int32)
+    p = pa.pa_plan(c, ctx)
+    assert p.work.shape[0] == 6
+    assert sorted(set((p.work[:, 5] - p.work[:, 4]).tolist())) == [9, 20]
+    # three sequences of 20 blocks: c_bal = ceil(60/8) = 8 gives 9 items in 3
+    # waves (24); 9 keeps 9 items (27); 10 gives 6 items in 2 waves (20), and
+    # nothing up to 16 is cheaper
+    c = cfg(batch=3, **base)
+    p = pa.pa_plan(c, np.full(3, 20 * 128, np.int32))
+    assert p.work.shape[0] == 6 and set((p.work[:, 5] - p.work[:, 4]).tolist()) == {10}
+    # already a single wave at c0 (one sequence of 20 blocks on 8 SMs:
+    # c0 = max(ceil(20/16), 4) = 4, 5 items): a longer chunk only costs
+    c = cfg(batch=1, **dict(base, num_sms=8))
+    p = pa.pa_plan(c, np.full(1, 20 * 128, np.int32))
+    assert p.work.shape[0] == 5 and set((p.work[:, 5] - p.work[:, 4]).tolist()) == {4}
+    # the same configurations through the oracle's restatement of the rule
+    for b, ctx in ((6, np.full(6, 2560, np.int32)),
+                   (6, np.array([2560] * 5 + [1152], np.int32)), (3, np.full(3, 2560, np.int32))):
+        cc = cfg(batch=b, **base)
+        work, comb, _ = oracle_plan(oracle_mod, cc, ctx, None)
+        hp = pa.pa_plan(cc, ctx)
+        assert np.array_equal(work, hp.work) and np.array_equal(comb, hp.combine)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_wave_fit_matches_oracle_with_few_sms(lib, oracle_mod, seed):
+    """Wide tiles on few SMs, where the wave fit moves the chunk most often:
+    pa_plan equals the oracle's planner bit for bit."""
+    rng = np.random.default_rng(700 + seed)
+    G = int(rng.choice([16, 32, 64]))
+    Hk = int(rng.choice([1, 2]))
+    hk = int(rng.choice([64, 128, 576]))
+    hv = 512 if hk == 576 else hk
+    bs = int(rng.choice([16, 64, 128]))
+    maxq = int(rng.choice([1, 1, 3]))
+    B = int(rng.integers(1, 60))
+    ctx = rng.integers(1, 6000, size=B).astype(np.int32)
+    ql = None if maxq == 1 else rng.integers(1, maxq + 1, size=B).astype(np.int32)
+    if ql is not None:
+        ctx = np.maximum(ctx, ql)
+    c = cfg(batch=B, num_heads=G * Hk, kv_heads=Hk, head_size_k=hk, head_size_v=hv,
+            block_size=bs, max_seqlen_q=maxq, max_blocks_per_seq=int(-(-ctx.max() // bs)),
+            chunk_blocks=0, num_sms=int(rng.choice([1, 3, 7, 16, 152])))
+    hp = pa.pa_plan(c, ctx, ql)
+    work, comb, _ = oracle_plan(oracle_mod, c, ctx, ql)
+    assert np.array_equal(work, hp.work) and np.array_equal(comb, hp.combine)
+    check_partition(c, ctx, ql, hp)
+
+
 def test_two_call_convention_and_small_buffers(lib):
     import ctypes
     c = cfg(batch=3, chunk_blocks=2)
