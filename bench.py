@@ -75,6 +75,8 @@ KERNEL_SOURCES = {
     "fma_decode_kernel": ["pa_decode_fma.cuh"],
     "tc_decode_kernel": ["pa_decode_tc.cuh", "pa_decode_tc.cu"],
     "pf_attn_kernel": ["pa_prefill_tc.cuh", "pa_prefill_tc.cu", "pa_decode_tc.cuh"],
+    "pf_pair_kernel": ["pa_prefill_pair.cuh", "pa_prefill_pair.cu", "pa_prefill_tc.cuh",
+                       "pa_decode_tc.cuh"],
 }
 COMMON_SOURCES = ["pa_device.cuh", "pa_warp_pipe.cuh"]
 
@@ -106,7 +108,7 @@ def dominant_kernel(cfg):
     """The attention kernel pa_forward picks for this configuration."""
     rows = (cfg.num_heads // cfg.kv_heads) * max(1, cfg.max_seqlen_q)
     if rows > 64 and cfg.head_size_k == cfg.head_size_v and cfg.head_size_k in (64, 128):
-        return "pf_attn_kernel"
+        return "pf_pair_kernel" if rows > 128 else "pf_attn_kernel"
     if rows > 8:
         return "tc_decode_kernel"
     mma = (cfg.head_size_k == cfg.head_size_v and cfg.head_size_k in (64, 128, 256, 512)) or \

@@ -89,6 +89,7 @@ typedef enum pa_mask_type {
 #define PA_FMA_MAX_ROWS 8
 #define PA_TC_TILE_ROWS 64
 #define PA_PF_TILE_ROWS 128
+#define PA_PF_PAIR_ROWS 256
 #define PA_STATUS_BYTES 256
 
 /* Status bits written by the kernels into the first word of the workspace. */
@@ -140,6 +141,9 @@ typedef struct pa_config {
  * token-major: row r is query token i = r / G of head h = kvh * G + r % G.
  * A launch uses one tile height TR for every sequence:
  *   TR = G * max_seqlen_q   if that is <= PA_FMA_MAX_ROWS (CUDA-core path)
+ *   TR = PA_PF_PAIR_ROWS    if G * max_seqlen_q > PA_PF_TILE_ROWS and
+ *                           hk = hv in {64, 128}  (prefill: two query tiles
+ *                                                  sharing each K/V tile)
  *   TR = PA_PF_TILE_ROWS    if G * max_seqlen_q > PA_TC_TILE_ROWS and
  *                           hk = hv in {64, 128}       (prefill-shaped tiles)
  *   TR = PA_TC_TILE_ROWS    otherwise                      (tensor-core path)

@@ -193,8 +193,9 @@ static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 /*
  * The work-list rule, restated from its written definition:
- *   tile height    TR = G * maxq if that is at most 8; else 128 if G * maxq > 64
- *                  and hk = hv in {64, 128}; else 64
+ *   tile height    TR = G * maxq if that is at most 8; else, when hk = hv in
+ *                  {64, 128}, 256 if G * maxq > 128 and 128 if G * maxq > 64;
+ *                  else 64
  *   tiles          QT_b = ceil(G * q_b / TR)
  *   blocks         NB_b = ceil(L_b / bs)
  *   chunk          c = chunk_blocks if positive, else
@@ -221,7 +222,7 @@ int oracle_plan(int batch, int num_heads, int kv_heads, int hk, int hv, int bloc
   const int64_t maxq = max_seqlen_q > 0 ? max_seqlen_q : 1;
   int64_t TR = 64;
   if (G * maxq <= 8) TR = G * maxq;
-  else if (G * maxq > 64 && hk == hv && (hk == 64 || hk == 128)) TR = 128;
+  else if (G * maxq > 64 && hk == hv && (hk == 64 || hk == 128)) TR = G * maxq > 128 ? 256 : 128;
   int64_t c;
   if (chunk_blocks > 0) {
     c = chunk_blocks;

@@ -36,6 +36,7 @@ PA_STATUS_BYTES = 256
 PA_FMA_MAX_ROWS = 8
 PA_TC_TILE_ROWS = 64
 PA_PF_TILE_ROWS = 128
+PA_PF_PAIR_ROWS = 256
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_plan", "pa_forward", "pa_forward_noalloc", "pa_plan_bounds", "pa_plan_device",
@@ -293,7 +294,7 @@ def list_capacity(cfg: pa_config) -> tuple[int, int]:
     if rows <= PA_FMA_MAX_ROWS:
         tr = rows
     elif rows > PA_TC_TILE_ROWS and pf_heads:
-        tr = PA_PF_TILE_ROWS
+        tr = PA_PF_PAIR_ROWS if rows > PA_PF_TILE_ROWS else PA_PF_TILE_ROWS
     else:
         tr = PA_TC_TILE_ROWS
     tiles = cfg.batch * cfg.kv_heads * (-(-rows // tr))

@@ -12,6 +12,7 @@
 #include "pa_combine.cuh"
 #include "pa_decode_mma.cuh"
 #include "pa_decode_tc.cuh"
+#include "pa_prefill_pair.cuh"
 #include "pa_prefill_tc.cuh"
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -249,7 +250,7 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
       case 4: err = launch_fma<4>(tmk, tmv, P, n_items, stream); break;
       default: err = launch_fma<8>(tmk, tmv, P, n_items, stream); break;
     }
-  } else if (TR == PA_PF_TILE_ROWS) {
+  } else if (TR == PA_PF_TILE_ROWS || TR == PA_PF_PAIR_ROWS) {
     // rows meet many keys (prefill, or more than one 64-row tile per kv head):
     // 128-token key tiles, boxes of min(block_size, 128) tokens, both 64-dim
     // halves in one box at 128
@@ -259,7 +260,8 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
     if (!cache_map_3d(&tmk, key_cache, c, hk, rows, halves) ||
         !cache_map_3d(&tmv, value_cache, c, kv_shared ? hk : hv, rows, halves))
       return PA_ERR_CUDA;
-    err = launch_pf(tmk, tmv, P, n_items, stream);
+    err = TR == PA_PF_PAIR_ROWS ? launch_pf_pair(tmk, tmv, P, n_items, stream)
+                                : launch_pf(tmk, tmv, P, n_items, stream);
   } else {
     // 64-row tiles on the tcgen05 kernel: boxes of min(block_size, 64) tokens
     if (!tc_supported(hk, hv)) return PA_ERR_UNSUPPORTED;

@@ -18,13 +18,16 @@ pa_status validate_config(const pa_config* cfg);
 inline int64_t max_q(const pa_config& c) { return c.max_seqlen_q > 0 ? c.max_seqlen_q : 1; }
 
 // Tile height of a launch: every row of a (b, kv head) pair in one CTA when
-// the group is small enough for the CUDA-core kernel, else 64-row tiles.
+// the group is small enough for the CUDA-core kernel; for 64/128-dim heads
+// with more than 64 rows, 128-row tiles, or 256 (two 128-row query tiles
+// sharing K and V) past 128 rows; else 64-row tiles.
 inline int64_t tile_rows(const pa_config& c) {
   const int64_t g = c.num_heads / c.kv_heads;
   const int64_t r = g * max_q(c);
   if (r <= PA_FMA_MAX_ROWS) return r;
   const bool pf_heads = c.head_size_k == c.head_size_v && (c.head_size_k == 64 || c.head_size_k == 128);
-  return (r > PA_TC_TILE_ROWS && pf_heads) ? PA_PF_TILE_ROWS : PA_TC_TILE_ROWS;
+  if (r > PA_TC_TILE_ROWS && pf_heads) return r > PA_PF_TILE_ROWS ? PA_PF_PAIR_ROWS : PA_PF_TILE_ROWS;
+  return PA_TC_TILE_ROWS;
 }
 
 #ifdef __CUDACC__

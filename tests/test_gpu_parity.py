@@ -195,9 +195,9 @@ TC_CASES = {
     # block_size 256: a tile is half a block
     "tc_bs256": lambda: W.make_workload("tc256", context_lens=[600, 256, 257], num_heads=16,
                                         kv_heads=1, head_size_k=128, block_size=256, seed=35),
-    # prefill (q = L) with the causal mask: 64-token row tiles skip the keys
-    # past their last token; 1-block chunks make splits that lie wholly past
-    # it (empty, weight zero in the combine)
+    # prefill (q = L) with the causal mask: row tiles skip the keys past their
+    # last token; 1-block chunks make splits that lie wholly past it (empty,
+    # weight zero in the combine)
     "tc_prefill_split": lambda: W.make_workload("pf", context_lens=[300, 129], q_seqlens=[300, 129],
                                                 num_heads=2, kv_heads=2, head_size_k=128,
                                                 block_size=64, mask_type=W.MASK_NORM_COMPRESS,
@@ -206,6 +206,22 @@ TC_CASES = {
                                               num_heads=8, kv_heads=2, head_size_k=128,
                                               block_size=32, mask_type=W.MASK_NORM_COMPRESS,
                                               seed=41),
+    # 128-row tiles (65-128 rows per kv head): causal prefill of up to 128
+    # tokens, and 64-dim heads with ALiBi; every other prefill case here has
+    # more than 128 rows and runs as 256-row tiles (two query tiles per CTA)
+    "pf128_prefill": lambda: W.make_workload("pf128", context_lens=[100, 300, 128],
+                                             q_seqlens=[100, 128, 128], num_heads=3, kv_heads=3,
+                                             head_size_k=128, block_size=64,
+                                             mask_type=W.MASK_NORM_COMPRESS, seed=45),
+    "pf128_hd64_alibi": lambda: W.make_workload("pf128a", context_lens=[77, 400], q_seqlens=[50, 64],
+                                                num_heads=4, kv_heads=2, head_size_k=64,
+                                                block_size=16, mask_type=W.MASK_ALIBI, seed=46),
+    # a 256-row tile whose second query tile holds only part of the rows, with
+    # the causal mask past 2048 (L = 2300, q = 200)
+    "pf256_ragged_long": lambda: W.make_workload("pf256", context_lens=[2300, 60], q_seqlens=[200, 60],
+                                                 num_heads=2, kv_heads=2, head_size_k=128,
+                                                 block_size=128, mask_type=W.MASK_NORM_COMPRESS,
+                                                 seed=47),
     # many-row tiles (prefill kernel): head size 64, ALiBi, 16-token blocks
     "pf_hd64_alibi_bs16": lambda: W.make_workload("pf64", context_lens=[333, 90], q_seqlens=[40, 90],
                                                   num_heads=8, kv_heads=4, head_size_k=64,
