@@ -390,27 +390,28 @@ __global__ void __launch_bounds__(kPpThreads, 1) pf_pair_kernel(
 #pragma unroll
           for (int i = 0; i < kPfTok; ++i) x[i] = i < jend ? x[i] : -INFINITY;
         }
-        float t4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float t4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four max chains
 #pragma unroll
         for (int i = 0; i < kPfTok; ++i) t4[i & 3] = fmaxf(t4[i & 3], x[i]);
         const float tmax = fmaxf(fmaxf(t4[0], t4[1]), fmaxf(t4[2], t4[3])) * P.scale_log2;
         if (!settle(tmax)) { ok = false; break; }
-        const float sc = P.scale_log2, nm = -m_ref;
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four independent sum chains
+        // exponents and sums on packed fp32 pairs (two lanes per instruction)
+        const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
+        const float2 nm2 = make_float2(-m_ref, -m_ref), one2 = make_float2(1.f, 1.f);
+        float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // four sum chains
 #pragma unroll
         for (int cc = 0; cc < kPfTok / 32; ++cc) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float e0 = ex2(fmaf(x[cc * 32 + 2 * i], sc, nm));
-            const float e1 = ex2(fmaf(x[cc * 32 + 2 * i + 1], sc, nm));
-            ps[(2 * i) & 3] += e0;
-            ps[(2 * i + 1) & 3] += e1;
+            const float2 a = fma2(make_float2(x[cc * 32 + 2 * i], x[cc * 32 + 2 * i + 1]), sc2, nm2);
+            const float e0 = ex2(a.x), e1 = ex2(a.y);
+            ps2[i & 1] = fma2(make_float2(e0, e1), one2, ps2[i & 1]);
             pk[i] = pack_half2(e0, e1);
           }
           tmem_st16u(sbuf + cc * 16, pk);
         }
-        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        l += (ps2[0].x + ps2[0].y) + (ps2[1].x + ps2[1].y);
         tmem_wait_st();
       } else {
         // Pass 1, 32 columns at a time: scores in base 2 with the bias,
