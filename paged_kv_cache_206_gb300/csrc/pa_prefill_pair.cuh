@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kPpThreads, 1) pf_pair_kernel(
       const int st = tid - 128 - grp * 128;
       uint8_t* qt = q_s + grp * Cfg::kQt;
       constexpr int kChunks = kPpQRows * (HD / 8);
-      constexpr int kPer = kChunks / 128, kRound = kPer < 8 ? kPer : 8;
+      constexpr int kPer = kChunks / 128, kRound = kPer;  // every load in flight at once
 #pragma unroll
       for (int k0 = 0; k0 < kPer; k0 += kRound) {
         uint4 v[kRound];  // every load of the round before any store
