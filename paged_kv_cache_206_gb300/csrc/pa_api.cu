@@ -251,9 +251,10 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
       default: err = launch_fma<8>(tmk, tmv, P, n_items, stream); break;
     }
   } else if (TR == PA_PF_TILE_ROWS || TR == PA_PF_PAIR_ROWS) {
-    // rows meet many keys (prefill, or more than one 64-row tile per kv head):
-    // 128-token key tiles, boxes of min(block_size, 128) tokens, both 64-dim
-    // halves in one box at 128
+    // rows meet many keys (more than one 64-row tile per kv head: 128-row
+    // tiles, or 256-row tiles of two query tiles for prefill): 128-token key
+    // tiles, boxes of min(block_size, 128) tokens, both 64-dim halves in one
+    // box at 128
     const int rows = c.block_size < 128 ? c.block_size : 128;
     const int halves = rows == 128 ? hk / 64 : 1;
     CUtensorMap tmk, tmv;

@@ -4,31 +4,6 @@
 // QK^T and PV real dense tiles. PagedAttentionOperation semantics (block
 // tables, context lengths, mask/bias); split/merge as in the metadata page.
 //
-// One CTA per work item, 10 warps:
-//   warp 0     TMA producer: 128-token x 64-dim boxes (16 KB, 128-byte swizzle)
-//              of K then V of each 128-token tile into a ring of 8 slots.
-//   warp 1     allocates TMEM; one thread issues the MMAs:
-//                S^T[128 tok x 64 rows]  = K . Q^T           (A, B K-major)
-//                O^T[hv x 64 rows]      += V^T . P^T         (A, B MN-major)
-//              with S^T and O^T accumulated in TMEM (fp32).
-//   warps 2-9  softmax: two warps per TMEM lane quarter; thread = token (TMEM
-//              lane) and one half (32) of the 64 rows, its scores in registers.
-//              Probabilities are taken against a per-row reference max that is
-//              recomputed exactly (warp max + 4-quarter exchange) only when some
-//              score exceeds it by more than 2^8 -- in practice the first tile;
-//              O^T and the sums are rescaled then (exact: the final
-//              normalisation uses the same reference). Row sums accumulate per
-//              token and are reduced across tokens once, at the end. P^T (fp16)
-//              goes to shared memory in the MN-major swizzled layout the PV MMA
-//              reads. Epilogue: thread = output dim, O^T / l from TMEM to out.
-// Every wait is bounded; on a timeout the CTA records PA_STATUS_BIT_TIMEOUT,
-// lets its copies land, frees its TMEM and exits.
-// Split-KV paged decode on the 5th-generation tensor cores (tcgen05 + TMEM) for
-// 64-row query tiles: a wide GQA/MQA group (e.g. 64 query heads sharing one kv
-// head of 512 dims, the shape of SparseAttnSharedkvMetadata's operator) makes
-// QK^T and PV real dense tiles. PagedAttentionOperation semantics (block
-// tables, context lengths, mask/bias); split/merge as in the metadata page.
-//
 // The KV range of a work item is cut into 64-token tiles. One CTA per item,
 // 12 warps:
 //   warp 0     K producer: 3-D TMA boxes of 64 tokens x 128 dims (16 KB, two

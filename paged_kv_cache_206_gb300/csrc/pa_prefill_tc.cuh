@@ -1,11 +1,12 @@
-// Paged attention for tiles whose rows meet many keys (prefill, q = L, and any
-// launch whose group rows G * max_q exceed one 64-row tile), on the tcgen05
-// tensor cores. Same operation, work item and split/merge contract as the
-// decode kernels (PagedAttentionOperation semantics; task list and FlashDecode
-// merge of the SparseAttnSharedkvMetadata page); a different tile shape.
+// Paged attention for 128-row tiles whose rows meet many keys (launches whose
+// group rows G * max_q are 65 to 128 with 64/128-dim heads: wide groups, short
+// prefill; beyond 128 rows the 256-row kernel of pa_prefill_pair.cuh takes
+// over), on the tcgen05 tensor cores. Same operation, work item and
+// split/merge contract as the decode kernels (PagedAttentionOperation
+// semantics; task list and FlashDecode merge of the SparseAttnSharedkvMetadata
+// page); a different tile shape.
 //
-// One CTA per work item (a 128-row tile: the work list uses 128-row tiles
-// for these launches), 128-token key tiles, 12 warps:
+// One CTA per work item (a 128-row tile), 128-token key tiles, 12 warps:
 //   warps 0, 2 TMA producers of K and of V: each key tile as 3-D boxes
 //              (128-byte swizzle) into 3-slot K and V rings.
 //   warp 1     allocates TMEM; one thread issues S = Q . K^T (M=128 rows,
