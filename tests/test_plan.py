@@ -125,6 +125,30 @@ def test_auto_chunk_rule_values(lib):
     assert set((p.work[:, 5] - p.work[:, 4]).tolist()) == {8}
 
 
+def test_tile_height_rule(lib, oracle_mod):
+    """Row tiles by the group rows G * max_q and the head sizes: every row of
+    a (sequence, kv head) up to 8 rows; 64-row tiles; for hk = hv in {64, 128}
+    128-row tiles past 64 rows and 256-row tiles past 128."""
+    cases = [  # (heads, kv heads, hk, hv, max_q) -> expected tile height
+        ((8, 1, 128, 128, 1), 8), ((16, 1, 128, 128, 1), 64), ((16, 1, 128, 128, 4), 64),
+        ((16, 1, 128, 128, 5), 128), ((32, 1, 128, 128, 4), 128), ((1, 1, 64, 64, 128), 128),
+        ((1, 1, 64, 64, 129), 256), ((32, 1, 128, 128, 5), 256), ((64, 1, 512, 512, 1), 64),
+        ((16, 1, 256, 256, 9), 64), ((16, 1, 576, 512, 9), 64), ((2, 1, 128, 128, 300), 256),
+    ]
+    for (H, Hk, hk, hv, q), tr in cases:
+        c = cfg(batch=1, num_heads=H, kv_heads=Hk, head_size_k=hk, head_size_v=hv,
+                block_size=64, max_seqlen_q=q, max_blocks_per_seq=40, chunk_blocks=100)
+        rows = (H // Hk) * q
+        ql = np.array([q], np.int32) if q > 1 else None
+        p = pa.pa_plan(c, np.array([max(q, 300)], np.int32), ql)
+        got = int(p.work[0, 3] - p.work[0, 2])
+        assert got == min(tr, rows), ((H, Hk, hk, hv, q), got, tr)
+        assert p.work.shape[0] == -(-rows // tr)
+        work, _, _ = oracle_plan(oracle_mod, c, np.array([max(q, 300)], np.int32), ql)
+        assert np.array_equal(work, p.work)
+        assert pa.list_capacity(c)[1] == -(-rows // tr)
+
+
 def test_auto_chunk_wave_fit(lib, oracle_mod):
     """Row tiles above 8 rows run one CTA per SM, so the automatic chunk is
     then refined: of c0 .. min(2 c0, c0 + 31, max(c0, max NB)) the chunk with
