@@ -12,8 +12,8 @@
 //              tile's causal range has one reader).
 //   warp 1     allocates TMEM; one thread issues, for each query tile g,
 //              S_g = Q_g . K^T (M=128 rows, N=128 tokens, K-major operands)
-//              and O_g += P_g . V (A = P_g from TMEM, B = V MN-major), each as
-//              soon as its inputs are ready. S_g(n + 1) overwrites the
+//              and O_g += P_g . V (A = P_g from TMEM, B = V MN-major) in a
+//              fixed order with blocking waits. S_g(n + 1) overwrites the
 //              columns that held P_g(n), so it is issued after PV_g(n); the
 //              other tile's chain fills the tensor pipe meanwhile.
 //   warps 4-11 softmax group g (warps 4-7: g = 0, 8-11: g = 1) owns query tile
