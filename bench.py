@@ -42,6 +42,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TFLOPS = 1900.0
 FLUSH_BYTES = 512 << 20
+REF_BUDGET_S = 150.0  # the reference arm's whole run, about
 
 
 def parse():
@@ -253,6 +254,27 @@ def reduce_over_ranks(maxes, sums, world, device):
     return t.tolist(), u.tolist()
 
 
+def reference_sample(w, nseq: int, nkv: int):
+    """The first nseq sequences of w restricted to its first nkv kv heads (and
+    their query heads): a smaller batch of the same shapes and values, the
+    reference arm's per-step sample."""
+    import dataclasses
+    G = w.num_heads // w.kv_heads
+    H = nkv * G
+    nq = int(w.q_seqlens[:nseq].sum())
+    mask = w.mask
+    if mask is not None and mask.ndim == 3:  # MASK_TYPE_NORM: one mask per sequence
+        mask = np.ascontiguousarray(mask[:nseq])
+    # (a shared-KV workload's value_cache already holds the first hv dims of K)
+    kc = np.ascontiguousarray(w.key_cache[:, :, :nkv])
+    vc = np.ascontiguousarray(w.value_cache[:, :, :nkv])
+    return dataclasses.replace(
+        w, num_heads=H, kv_heads=nkv, context_lens=w.context_lens[:nseq].copy(),
+        q_seqlens=w.q_seqlens[:nseq].copy(), block_tables=w.block_tables[:nseq].copy(),
+        query=np.ascontiguousarray(w.query[:nq, :H]), key_cache=kc, value_cache=vc, mask=mask,
+        alibi_slopes=None if w.alibi_slopes is None else w.alibi_slopes[:H].copy())
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -261,32 +283,41 @@ def run_reference(args):
     oracle.build()
     w = workload(args.workload, 0, args.chunk_blocks)
     cores = len(os.sched_getaffinity(0))
-    # bounded sample per step: the first n sequences, n sized for ~0.5 s per step
+    # Bounded sample per step, sized so that the whole run (warm-up and timed
+    # steps) takes about REF_BUDGET_S, at most 0.5 s a step: the first nseq
+    # sequences with the first nkv kv heads. The oracle works on (sequence, kv
+    # head) units, one thread each; one unit is the smallest sample.
+    unit = reference_sample(w, 1, 1)
     t0 = time.perf_counter()
-    oracle.attention(w, subset=[0], threads=cores)
-    one = max(time.perf_counter() - t0, 1e-4)
-    n = max(1, min(w.batch, int(0.5 * min(cores, w.batch) / one)))
-    sub = list(range(n))
-    per = w.head_size_k + (0 if w.shared_kv else w.head_size_v)
-    kv = int(w.context_lens[sub].astype(np.int64).sum()) * w.kv_heads * per * 2
+    oracle.attention(unit, threads=1)
+    one = max(time.perf_counter() - t0, 1e-5)
+    per_step = min(0.5, REF_BUDGET_S / max(1, args.steps + args.warmup))
+    units = max(1, int(per_step * cores / one))
+    nseq = min(w.batch, units)
+    nkv = min(w.kv_heads, max(1, units // nseq))
+    smp = reference_sample(w, nseq, nkv)
+    kv = smp.kv_bytes()
     used = 1
     for _ in range(args.warmup):
-        _, used = oracle.attention(w, subset=sub, threads=cores)
+        _, used = oracle.attention(smp, threads=cores)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _, used = oracle.attention(w, subset=sub, threads=cores)
+        _, used = oracle.attention(smp, threads=cores)
         times.append(time.perf_counter() - t0)
     dt = statistics.mean(times)
     value = kv / dt / 1e9
+    sample = (f"{nseq} of {w.batch} sequences x {nkv} of {w.kv_heads} kv heads per step, "
+              f"fp64 C oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "sample_sequences": n, "batch": w.batch},
+        "config": {"workload": args.workload, "sample_sequences": nseq, "sample_kv_heads": nkv,
+                   "batch": w.batch},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": int(used), "kind": "oracle",
-                         "sample": f"{n} of {w.batch} sequences per step, fp64 C oracle"},
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

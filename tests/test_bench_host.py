@@ -66,3 +66,30 @@ def test_percentiles_nearest_rank():
     p = bench.percentiles(xs)
     assert p == {"median": 6, "p10": 2, "p90": 10}
     assert bench.percentiles([5.0]) == {"median": 5.0, "p10": 5.0, "p90": 5.0}
+
+
+@pytest.mark.parametrize("make", [
+    lambda: W.tiny_decode(seed=3),
+    lambda: W.make_workload("spec", context_lens=[40, 300, 90], q_seqlens=[2, 4, 3], num_heads=8,
+                            kv_heads=4, head_size_k=64, block_size=16,
+                            mask_type=W.MASK_NORM_COMPRESS, seed=4),
+    lambda: W.make_workload("alibi", context_lens=[70, 20], num_heads=6, kv_heads=3,
+                            head_size_k=64, block_size=16, mask_type=W.MASK_ALIBI, seed=5),
+    lambda: W.make_workload("shared", context_lens=[50, 33, 80], num_heads=8, kv_heads=2,
+                            head_size_k=128, head_size_v=64, block_size=16, seed=6,
+                            shared_kv=True),
+])
+def test_reference_sample_is_a_slice_of_the_workload(oracle_mod, make):
+    """The reference arm's per-step sample (first sequences x first kv heads)
+    is the same attention problem restricted: the oracle on it equals the
+    matching rows and heads of the oracle on the whole batch."""
+    w = make()
+    full, _ = oracle_mod.attention(w, threads=2)
+    G = w.num_heads // w.kv_heads
+    for nseq, nkv in ((1, 1), (w.batch, 1), (w.batch - 1, w.kv_heads)):
+        smp = bench.reference_sample(w, nseq, nkv)
+        got, _ = oracle_mod.attention(smp, threads=2)
+        nq = int(w.q_seqlens[:nseq].sum())
+        assert np.array_equal(got, full[:nq, :nkv * G])
+        per = w.head_size_k + (0 if w.shared_kv else w.head_size_v)
+        assert smp.kv_bytes() == int(w.context_lens[:nseq].sum()) * nkv * per * 2
