@@ -57,6 +57,12 @@ def test_half_decode_all_bit_patterns(oracle_mod):
          mask_type=W.MASK_NORM),
     dict(context_lens=[6, 33, 70], q_seqlens=[3, 1, 4], num_heads=6, kv_heads=3,
          head_size_k=16, mask_type=W.MASK_NORM, block_size=32),
+    # the MLA shape: 576-dim K rows whose first 512 dims are V (shared cache)
+    dict(context_lens=[5, 70], num_heads=4, kv_heads=1, head_size_k=576, head_size_v=512,
+         shared_kv=True, std=0.5),
+    # prefill-shaped rows (q = L) with the compressed mask, 64-dim heads
+    dict(context_lens=[40, 17], q_seqlens=[40, 17], num_heads=2, kv_heads=2, head_size_k=64,
+         mask_type=W.MASK_NORM_COMPRESS),
 ])
 def test_oracle_matches_brute_force(oracle_mod, case):
     w = small(**case)
