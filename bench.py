@@ -1,23 +1,33 @@
 """Benchmark: paged-attention effective KV HBM GB/s and query tokens/s.
 
-One step is one pass of the whole device path over one synthetic batch: the
-attention kernel over the planned work list plus the split-KV combine. The
-work list comes from pa_plan before the timed region (it is host code, timed
-separately as plan_us). The end-to-end number (`e2e`) starts from pinned host
-buffers: each timed step replays one recorded CUDA graph that copies the
-step's inputs to the device, plans on the device, runs attention and combine
+One step is one pass of the whole device path over one synthetic batch:
+pa_forward over the planned work list (the attention kernel, then the split-KV
+combine kernel when the plan has split tiles). The work list comes from
+pa_plan before the timed region (host code, timed separately as plan_us). The end-to-end number (`e2e`) starts from
+pinned host buffers: each timed step replays one recorded CUDA graph that
+copies the step's inputs to the device, plans on the device, runs attention
 and copies the output back, and the host waits for it. The same step planned
-on the host with direct launches is reported beside it (`e2e.host_planned`).
+on the host with direct launches is reported beside it (`e2e.host_planned`),
+and the graph's stages are timed one by one with CUDA events
+(`e2e.breakdown_us`).
 
-Default workload: GQA decode, B=64, H=32, Hk=8, hk=hv=128, block_size=128,
-context lengths uniform in [1, 4096], one query token per sequence, seed 0.
-Before every timed step the 129 MB L2 is flushed outside the timed events (a
-512 MB buffer is written, then half of it read back so the write-backs of the
-flush's dirty lines also happen before the events), so every step reads the KV
-cache from HBM.
+One run measures every workload of the benchmark table (`configs`): tiny,
+GQA, parallel/speculative and ALiBi decode, long-context MQA split-KV, plus
+MLA-style shared-KV decode and causal prefill. The headline line is ALiBi
+decode (B=128, H=Hk=40, hk=hv=128, block_size=128, lengths uniform in
+[1, 2048], ALiBi slopes), the largest single-GPU workload (2.62 GB of KV);
+`--workload NAME` measures that one alone. Before every timed step the
+129 MB L2 is flushed outside the timed events (a 512 MB buffer is written,
+then half of it read back so the write-backs of the flush's dirty lines also
+happen before the events), so every step reads the KV cache from HBM.
+
+The HBM read ceiling is measured in the same process: a streaming read of
+2 GiB (pa_hbm_read_probe), best of several grid shapes. Roofline fractions are
+given against it (`frac_read`) and against the measured copy
+(`frac`, MEASURED_PEAKS.json).
 
 `--impl reference` times the CPU oracle on this machine's cores instead, on a
-bounded sample of the same workload, and prints the same JSON line.
+bounded sample of the headline workload, and prints the same JSON line.
 """
 from __future__ import annotations
 
@@ -43,18 +53,31 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TFLOPS = 1900.0
 FLUSH_BYTES = 512 << 20
 REF_BUDGET_S = 150.0  # the reference arm's whole run, about
+READ_PROBE_BYTES = 2 << 30
+
+# Every workload of the benchmark table, in the order of the table; the rows
+# the hot-path table marks "next" carry that tag. The headline is the largest
+# single-GPU workload.
+WORKLOADS = [("tiny_decode", "C1"), ("gqa_decode", "C2"), ("spec_decode", "C3"),
+             ("alibi_decode", "C4"), ("mqa_split", "C5"), ("mla_decode", "next"),
+             ("prefill_causal", "next")]
+HEADLINE = "alibi_decode"
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gqa_decode")
+    ap.add_argument("--workload", default=None,
+                    help="measure this workload alone (default: every workload, "
+                         f"headline {HEADLINE})")
     ap.add_argument("--chunk-blocks", type=int, default=None)
+    ap.add_argument("--config-steps", type=int, default=300,
+                    help="timed steps of each non-headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=100)
     return ap.parse_args()
 
 
@@ -115,6 +138,12 @@ def dominant_kernel(cfg):
     mma = (cfg.head_size_k == cfg.head_size_v and cfg.head_size_k in (64, 128, 256, 512)) or \
         (cfg.head_size_k, cfg.head_size_v) == (576, 512)
     return "mma_decode_kernel" if rows >= 2 and mma else "fma_decode_kernel"
+
+
+def launches_per_step(n_combine):
+    """Kernels one pa_forward launches: the attention kernel, plus the combine
+    kernel (its programmatic dependent) when the plan has split tiles."""
+    return 1 + (1 if n_combine else 0)
 
 
 class ClockSampler:
@@ -215,7 +244,7 @@ def percentiles(xs):
     return {"median": pick(0.5), "p10": pick(0.1), "p90": pick(0.9)}
 
 
-def cpu_baseline(w, max_seconds=20.0):
+def cpu_baseline(w, max_seconds=10.0):
     """The oracle on this machine's cores, on the whole batch or a prefix of it
     sized to stay within about max_seconds."""
     import oracle
@@ -281,7 +310,8 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    w = workload(args.workload, 0, args.chunk_blocks)
+    name = args.workload or HEADLINE
+    w = workload(name, 0, args.chunk_blocks)
     cores = len(os.sched_getaffinity(0))
     # Bounded sample per step, sized so that the whole run (warm-up and timed
     # steps) takes about REF_BUDGET_S, at most 0.5 s a step: the first nseq
@@ -314,13 +344,196 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "sample_sequences": nseq, "sample_kv_heads": nkv,
+        "config": {"workload": name, "sample_sequences": nseq, "sample_kv_heads": nkv,
                    "batch": w.batch},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": int(used), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def read_peak(dev, stream):
+    """HBM read bandwidth of this GPU: pa_hbm_read_probe over 2 GiB (more than
+    L2 holds), best mean over the grid shapes tried."""
+    import torch
+    import paged_kv_cache_206_gb300 as pa
+    buf = torch.empty(READ_PROBE_BYTES, dtype=torch.uint8, device=dev)
+    buf.fill_(1)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    best = None
+    for ctas in (1, 2, 4):
+        for _ in range(3):
+            pa.hbm_read_probe(buf, ctas, sink, stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(20)]
+        for a, b in ev:
+            a.record(stream)
+            pa.hbm_read_probe(buf, ctas, sink, stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        gbs = READ_PROBE_BYTES / (ms * 1e-3) / 1e9
+        if best is None or gbs > best["gbs"]:
+            best = {"gbs": gbs, "ctas_per_sm": ctas, "ms": ms}
+    del buf
+    return {"value": best["gbs"], "unit": "GB/s", "bytes": READ_PROBE_BYTES,
+            "ctas_per_sm": best["ctas_per_sm"],
+            "how": "pa_hbm_read_probe: 256-bit loads (L1 bypassed, L2 evict-first), "
+                   "512 threads a CTA, 8 loads in flight a thread; best of 1/2/4 CTAs per SM, "
+                   "mean of 20 launches each"}
+
+
+def measure(name, args, steps, dev, stream, flush, rank, peaks_, read_gbs, cpu_seconds):
+    """Every figure of one workload: the device step, its roofline, the end-to-end
+    step from host buffers (with its stages timed) and the oracle on the host."""
+    import torch
+    import paged_kv_cache_206_gb300 as pa
+
+    w = workload(name, rank, args.chunk_blocks)
+    db = pa.DeviceBatch(w, device=dev)
+    ql_host = None if np.all(w.q_seqlens == 1) else w.q_seqlens
+    plan_reps = 50
+    t0 = time.perf_counter()
+    for _ in range(plan_reps):
+        pa.pa_plan(db.cfg, w.context_lens, ql_host)
+    plan_us = (time.perf_counter() - t0) / plan_reps * 1e6
+    kv_bytes, qo_bytes = w.kv_bytes(), w.qo_bytes()
+    n_comb = db.plan.combine.shape[0]
+    n_items = db.plan.work.shape[0]
+    launches = launches_per_step(n_comb)
+
+    times = time_device(lambda: db.forward(stream), steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    st, bits = db.status(stream)
+    if st != pa.PA_OK:
+        raise RuntimeError(f"{name}: kernel status {pa.status_string(st)} ({bits})")
+    # the attention kernel alone (the roofline's kernel): the same launch
+    # without the combine list, which launches no combine kernel; without
+    # split tiles the step is that one launch
+    if n_comb:
+        def attention_only():
+            pa.pa_forward(db.cfg, db.query, db.key_cache, db.value_cache, db.block_tables,
+                          db.context_lens, db.q_seqlens, db.mask, db.alibi_slopes, db.work,
+                          None, db.workspace, db.out, stream)
+        kernel_ms = statistics.mean(time_device(attention_only, steps, 5, flush, stream))
+        db.forward(stream)
+    else:
+        kernel_ms = statistics.mean(times)
+
+    # end to end through the C ABI with host buffers: GraphStep replays one
+    # graph per step (copy in, device plan, attention, copy out; the host
+    # waits); HostStep plans on the host and launches directly; the graph's
+    # stages are also run directly with events between them
+    def fill(st_):
+        st_.query.copy_(torch.from_numpy(np.ascontiguousarray(w.query)))
+        st_.block_tables.copy_(torch.from_numpy(np.ascontiguousarray(w.block_tables)))
+        st_.context_lens.copy_(torch.from_numpy(np.ascontiguousarray(w.context_lens)))
+        if st_.q_seqlens is not None:
+            st_.q_seqlens.copy_(torch.from_numpy(np.ascontiguousarray(w.q_seqlens)))
+        return st_
+
+    gs = fill(pa.GraphStep(db.cfg, db.key_cache, db.value_cache, w.total_q, mask=db.mask,
+                           alibi_slopes=db.alibi_slopes))
+    hs = fill(pa.HostStep(db.cfg, db.key_cache, db.value_cache, w.total_q, mask=db.mask,
+                          alibi_slopes=db.alibi_slopes))
+
+    def time_host(fn, n):
+        for _ in range(min(5, n)):
+            fn()
+        out = []
+        for _ in range(n):
+            flush_l2(flush)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            out.append(time.perf_counter() - t0)
+        return out
+
+    e2e_t = time_host(gs.run, args.e2e_steps)
+    host_t = time_host(lambda: hs.run(stream), args.e2e_steps)
+    # the stages queue up behind the L2 flush (the step's stream waits for the
+    # flush's), so the events measure the GPU's time on each stage rather
+    # than the host's time to enqueue the next one
+    stage_ms = [[] for _ in range(4)]
+    for _ in range(max(1, args.e2e_steps // 2)):
+        torch.cuda.synchronize()
+        flush_l2(flush)
+        gs.stream.wait_stream(torch.cuda.current_stream(dev))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        gs.run_stages(ev)
+        for k in range(4):
+            stage_ms[k].append(ev[k].elapsed_time(ev[k + 1]))
+    if e2e_t:
+        for what, s_ in (("graph", gs.status()), ("host-planned", hs.status(stream))):
+            if s_[0] != pa.PA_OK:
+                raise RuntimeError(f"{name}: e2e {what} status {pa.status_string(s_[0])} ({s_[1]})")
+        db.forward(stream)
+        ref_out = db.out.cpu()
+        if not (torch.equal(gs.out, ref_out) and torch.equal(hs.out, ref_out)):
+            raise RuntimeError(f"{name}: end-to-end output differs from the device-resident run")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    ms = statistics.mean(times)
+    e2e_s = statistics.mean(e2e_t) if e2e_t else float("nan")
+    host_s = statistics.mean(host_t) if host_t else float("nan")
+    (ms_all, e2e_all, host_all), (kv_all, q_all) = reduce_over_ranks(
+        [ms, e2e_s, host_s], [kv_bytes, w.total_q], world, dev)
+    peak, tpeak, peak_kind = peaks_
+    value = kv_all / (ms_all * 1e-3) / 1e9
+    flops = w.attn_flops()
+    tensor_bound = flops / (kv_bytes + qo_bytes) > tpeak * 1e3 / peak
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": flops / (kernel_ms * 1e-3) / 1e12, "peak": tpeak,
+                "unit": "TFLOP/s", "flops": flops,
+                "bytes": "2*(hk+hv) flop per (query row, visible key), algorithmic"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+    else:
+        achieved = (kv_bytes + qo_bytes) / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "bytes": "KV + Q + O per launch (algorithmic)", "frac": achieved / peak,
+                "read_peak": read_gbs, "frac_read": achieved / read_gbs if read_gbs else None}
+    kernel = dominant_kernel(db.cfg)
+    base = None
+    if not args.no_cpu_baseline and world == 1:
+        base = cpu_baseline(w, cpu_seconds)
+    stages = [statistics.mean(x) * 1e3 for x in stage_ms]
+    res = {
+        "value": value, "unit": UNIT, "ms_per_step": ms_all, "steps": steps,
+        "step_ms": dict(percentiles(times), mean=ms),
+        "pct_of_nominal_8tbs": 100.0 * value / NOMINAL_HBM_GBS,
+        "query_tokens_per_s": q_all / (ms_all * 1e-3),
+        "config": {
+            "workload": name, "batch": w.batch, "num_heads": w.num_heads,
+            "kv_heads": w.kv_heads, "head_size_k": w.head_size_k, "head_size_v": w.head_size_v,
+            "block_size": w.block_size, "q_per_seq": w.max_seqlen_q, "mask_type": w.mask_type,
+            "shared_kv": w.shared_kv, "kv_bytes": kv_bytes, "qo_bytes": qo_bytes,
+            "items": n_items, "combines": n_comb, "chunk_blocks": db.cfg.chunk_blocks,
+            "l2": "flushed before every step, outside the events: 512 MB written, then 256 MB "
+                  "read back",
+            "plan_us": plan_us},
+        "roofline": dict(roof, traffic=ncu_traffic(kernel, name), peak_kind=peak_kind,
+                         kernel=kernel, kernel_ms=kernel_ms, launches_per_step=launches),
+        "e2e": None if not e2e_t else {
+            "value": kv_all / e2e_all / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": int(gs.h2d_bytes),
+            "d2h_bytes_per_step": int(gs.out.numel() * gs.out.element_size()),
+            "ms_per_step": e2e_all * 1e3,
+            "path": "GraphStep: one graph replay per step (copy in, device plan, attention, "
+                    "copy out), host waits",
+            "breakdown_us": {"h2d_copy": stages[0], "plan_device": stages[1],
+                             "attention": stages[2], "d2h_copy": stages[3],
+                             "how": "the graph's stages enqueued directly on its stream behind "
+                                    "the L2 flush, CUDA events between them"},
+            "host_planned": {"value": kv_all / host_all / 1e9, "ms_per_step": host_all * 1e3,
+                             "h2d_bytes_per_step": int(hs.last_h2d_bytes),
+                             "path": "HostStep: pa_plan on the host, direct launches"}},
+        "gpu_launches": steps * launches,
+        "cpu_baseline": base,
+    }
+    del gs, hs, db
+    torch.cuda.empty_cache()
+    return res
 
 
 def main():
@@ -345,161 +558,62 @@ def main():
         build_lib.build()
     if world > 1:
         dist.barrier()
-
-    w = workload(args.workload, rank, args.chunk_blocks)
-    t0 = time.perf_counter()
-    db = pa.DeviceBatch(w, device=dev)
-    plan_reps = 50
-    t0 = time.perf_counter()
-    for _ in range(plan_reps):
-        pa.pa_plan(db.cfg, w.context_lens, None if np.all(w.q_seqlens == 1) else w.q_seqlens)
-    plan_us = (time.perf_counter() - t0) / plan_reps * 1e6
+    pa.load_library()
 
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    kv_bytes = w.kv_bytes()
-    qo_bytes = w.qo_bytes()
-    n_comb = db.plan.combine.shape[0]
-    n_items = db.plan.work.shape[0]
-
-    def step():
-        db.forward(stream)
-
-    def decode_only():
-        pa.pa_forward(db.cfg, db.query, db.key_cache, db.value_cache, db.block_tables,
-                      db.context_lens, db.q_seqlens, db.mask, db.alibi_slopes, db.work, None,
-                      db.workspace, db.out, stream)
-
     props = torch.cuda.get_device_properties(dev)
     gpu_id = str(getattr(props, "uuid", local))
     if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) == 36:
         gpu_id = "GPU-" + gpu_id
+    peaks_ = peaks()
+    names = [args.workload] if args.workload else [n for n, _ in WORKLOADS]
+    headline = args.workload or HEADLINE
+    rows = dict(WORKLOADS)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    results = {}
     with ClockSampler(gpu_id) as clk:
-        times = time_device(step, args.steps, args.warmup, flush, stream)
+        rp = read_peak(dev, stream)
+        for n in names:
+            steps = args.steps if n == headline else min(args.steps, args.config_steps)
+            results[n] = measure(n, args, steps, dev, stream, flush, rank, peaks_, rp["value"],
+                                 10.0 if n == headline else 3.0)
+            results[n]["row"] = rows.get(n, "-")
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    st, bits = db.status(stream)
-    if st != pa.PA_OK:
-        raise RuntimeError(f"kernel status {pa.status_string(st)} ({bits})")
-
-    # the dominant kernel alone: the same launch without the combine pass
-    dec_times = time_device(decode_only, max(50, args.steps // 4), 5, flush, stream)
-
-    # end to end through the C ABI with host buffers. The step's inputs sit in
-    # one pinned host arena (query, block tables, lengths). GraphStep replays
-    # one recorded graph per step: the arena's copy to the device, the device
-    # planner, attention, combine and the output's copy back into pinned
-    # memory; the host waits for it. HostStep, timed beside it, plans on the
-    # host and launches each call directly.
-    def fill(st):
-        st.query.copy_(torch.from_numpy(np.ascontiguousarray(w.query)))
-        st.block_tables.copy_(torch.from_numpy(np.ascontiguousarray(w.block_tables)))
-        st.context_lens.copy_(torch.from_numpy(np.ascontiguousarray(w.context_lens)))
-        if st.q_seqlens is not None:
-            st.q_seqlens.copy_(torch.from_numpy(np.ascontiguousarray(w.q_seqlens)))
-        return st
-
-    gs = fill(pa.GraphStep(db.cfg, db.key_cache, db.value_cache, w.total_q, mask=db.mask,
-                           alibi_slopes=db.alibi_slopes))
-    hs = fill(pa.HostStep(db.cfg, db.key_cache, db.value_cache, w.total_q, mask=db.mask,
-                          alibi_slopes=db.alibi_slopes))
-
-    def time_host(fn):
-        for _ in range(min(5, args.e2e_steps)):
-            fn()
-        out = []
-        for _ in range(args.e2e_steps):
-            flush_l2(flush)
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            fn()
-            out.append(time.perf_counter() - t0)
-        return out
-
-    e2e_t = time_host(gs.run)
-    host_t = time_host(lambda: hs.run(stream))
-    h2d = gs.h2d_bytes
-    d2h = gs.out.numel() * gs.out.element_size()
-    if e2e_t:
-        for name, s_ in (("graph", gs.status()), ("host-planned", hs.status(stream))):
-            if s_[0] != pa.PA_OK:
-                raise RuntimeError(f"e2e {name} status {pa.status_string(s_[0])} ({s_[1]})")
-        db.forward(stream)
-        ref_out = db.out.cpu()
-        if not (torch.equal(gs.out, ref_out) and torch.equal(hs.out, ref_out)):
-            raise RuntimeError("end-to-end output differs from the device-resident run")
-
-    ms = statistics.mean(times)
-    step_pct = percentiles(times)
-    dec_ms = statistics.mean(dec_times)
-    e2e_s = statistics.mean(e2e_t) if e2e_t else float("nan")
-    host_s = statistics.mean(host_t) if host_t else float("nan")
-    (ms, dec_ms, e2e_s, host_s), (kv_all, qo_all, q_all) = reduce_over_ranks(
-        [ms, dec_ms, e2e_s, host_s], [kv_bytes, qo_bytes, w.total_q], world, dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    peak, tpeak, peak_kind = peaks()
-    value = kv_all / (ms * 1e-3) / 1e9
-    achieved = (kv_bytes + qo_bytes) / (dec_ms * 1e-3) / 1e9
-    flops = w.attn_flops()
-    # the bound: tensor when the arithmetic intensity passes the ridge point
-    tensor_bound = flops / (kv_bytes + qo_bytes) > tpeak * 1e3 / peak
-    if tensor_bound:
-        roof = {"bound": "tensor", "achieved": flops / (dec_ms * 1e-3) / 1e12, "peak": tpeak,
-                "unit": "TFLOP/s", "flops": flops,
-                "bytes": "2*(hk+hv) flop per (query row, visible key), algorithmic"}
-    else:
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "bytes": "KV + Q + O per launch (algorithmic)"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    kernel = dominant_kernel(db.cfg)
-    traffic = ncu_traffic(kernel, args.workload)
-    base = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w)
+    h = results[headline]
     line = {
         "metric": METRIC,
-        "value": value,
+        "value": h["value"],
         "unit": UNIT,
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": h["steps"],
         "warmup": args.warmup,
-        "ms_per_step": ms,
+        "ms_per_step": h["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f16",
         "data": "synthetic",
-        "config": {
-            "workload": args.workload, "batch": w.batch, "num_heads": w.num_heads,
-            "kv_heads": w.kv_heads, "head_size_k": w.head_size_k, "head_size_v": w.head_size_v,
-            "block_size": w.block_size, "q_per_seq": w.max_seqlen_q,
-            "mask_type": w.mask_type, "kv_bytes": kv_bytes, "qo_bytes": qo_bytes,
-            "items": n_items, "combines": n_comb, "chunk_blocks": db.cfg.chunk_blocks,
-            "l2": "flushed before every step, outside the events: 512 MB written, then 256 MB read back",
-            "plan_us": plan_us, "parallelism": f"replica x{world}" if world > 1 else "single",
-        },
-        "step_ms": dict(step_pct, mean=ms),
-        "query_tokens_per_s": q_all / (ms * 1e-3),
-        "pct_of_nominal_8tbs": 100.0 * value / NOMINAL_HBM_GBS,
-        "roofline": dict(roof, traffic=traffic, peak_kind=peak_kind, kernel=kernel,
-                         kernel_ms=dec_ms),
-        "e2e": None if not e2e_t else {
-            "value": kv_all / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_s * 1e3,
-            "path": "GraphStep: one graph replay per step (copy in, device plan, attention, "
-                    "combine, copy out), host waits",
-            "host_planned": {"value": kv_all / host_s / 1e9, "ms_per_step": host_s * 1e3,
-                             "h2d_bytes_per_step": int(hs.last_h2d_bytes),
-                             "path": "HostStep: pa_plan on the host, direct launches"}},
-        "gpu_launches": args.steps * (1 + (1 if n_comb else 0)),
+        "config": dict(h["config"], parallelism=f"replica x{world}" if world > 1 else "single"),
+        "step_ms": h["step_ms"],
+        "query_tokens_per_s": h["query_tokens_per_s"],
+        "pct_of_nominal_8tbs": h["pct_of_nominal_8tbs"],
+        "roofline": h["roofline"],
+        "e2e": h["e2e"],
+        "gpu_launches": h["gpu_launches"],
         "clocks": clk.summary(),
-        "cpu_baseline": base,
+        "cpu_baseline": h["cpu_baseline"],
+        "hbm_read_peak": rp,
+        "configs": results,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -244,7 +244,9 @@ pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens, const int32
  * Host-side errors return before anything is enqueued. Block-table entries
  * outside [0, num_blocks) are never dereferenced: the kernel skips their
  * copies, leaving the affected outputs undefined, and sets
- * PA_STATUS_BIT_BLOCK_INDEX, which pa_status_read reports.
+ * PA_STATUS_BIT_BLOCK_INDEX, which pa_status_read reports. Launches: the
+ * attention kernel, then, when n_combine > 0, the reduction kernel as its
+ * programmatic dependent.
  */
 pa_status pa_forward(const pa_config* cfg, const void* query, const void* key_cache,
                      const void* value_cache, const int32_t* block_tables,
@@ -273,8 +275,9 @@ pa_status pa_forward(const pa_config* cfg, const void* query, const void* key_ca
  *
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress) and caches it; make that first call
- * before any stream capture. Each call zeroes the array's status word on the
- * stream before launching. All calls on a device share the one array, so calls
+ * before any stream capture. Each call runs pa_forward's host-side checks
+ * first (a rejected call enqueues nothing and leaves `status` unwritten), then
+ * zeroes the array's status word on the stream before launching. All calls on a device share the one array, so calls
  * whose work overlaps on the GPU (other streams, other host threads) race.
  * Calls no cudaMalloc, cudaFree or allocating library routine.
  */
@@ -348,7 +351,8 @@ pa_status pa_forward_device_plan(const pa_config* cfg, const void* query, const 
 pa_status pa_status_clear(void* workspace, void* stream);
 
 /* Wait for stream, read the status word into *bits (may be NULL) and map it to
- * PA_OK, PA_ERR_TIMEOUT, PA_ERR_BLOCK_INDEX or PA_ERR_BUFFER_TOO_SMALL. */
+ * PA_OK, PA_ERR_TIMEOUT, PA_ERR_BLOCK_INDEX, PA_ERR_BUFFER_TOO_SMALL or
+ * PA_ERR_INVALID_ARG (PA_STATUS_BIT_PLAN). */
 pa_status pa_status_read(const void* workspace, void* stream, uint32_t* bits);
 
 /* Static description of a status code. */

@@ -38,10 +38,17 @@ PA_TC_TILE_ROWS = 64
 PA_PF_TILE_ROWS = 128
 PA_PF_PAIR_ROWS = 256
 
-# Every symbol include/pa.h declares.
+# Every symbol include/*.h declares (pa.h, the attention ABI; pa_probe.h, the
+# HBM read probe; pa_testing.h, the test hook).
 EXPORTS = ("pa_plan", "pa_forward", "pa_forward_noalloc", "pa_plan_bounds", "pa_plan_device",
-           "pa_forward_device_plan", "pa_status_clear", "pa_status_read", "pa_status_string")
+           "pa_forward_device_plan", "pa_status_clear", "pa_status_read", "pa_status_string",
+           "pa_hbm_read_probe", "pa_testing_set_wait_limit")
 PA_PLAN_COUNTS = 4
+
+PA_STATUS_BIT_BLOCK_INDEX = 1
+PA_STATUS_BIT_TIMEOUT = 2
+PA_STATUS_BIT_WORKSPACE = 4
+PA_STATUS_BIT_PLAN = 8
 
 # Size of the device array pa_forward_noalloc uses as its workspace.
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -107,6 +114,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.pa_status_read.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [ctypes.c_int]
+    lib.pa_hbm_read_probe.restype = ctypes.c_int
+    lib.pa_hbm_read_probe.argtypes = [P, sz, ctypes.c_int, P, P]
+    lib.pa_testing_set_wait_limit.restype = ctypes.c_int
+    lib.pa_testing_set_wait_limit.argtypes = [ctypes.c_longlong]
     if path == LIB:
         _lib = lib
     return lib
@@ -211,6 +222,20 @@ def pa_forward_noalloc(cfg: pa_config, query, key_cache, value_cache, block_tabl
                                 int(workspace_bytes), _tptr(status), _tptr(out),
                                 _stream_handle(stream))
     _check(st, "pa_forward_noalloc")
+
+
+def hbm_read_probe(buf, ctas_per_sm: int, sink, stream=None) -> None:
+    """Enqueue one streaming read of the CUDA tensor ``buf`` (pa_hbm_read_probe);
+    ``sink`` is a one-element CUDA int32/uint32 tensor the probe XORs into."""
+    _check(load_library().pa_hbm_read_probe(_tptr(buf), buf.numel() * buf.element_size(),
+                                            int(ctas_per_sm), _tptr(sink),
+                                            _stream_handle(stream)), "pa_hbm_read_probe")
+
+
+def testing_set_wait_limit(cycles: int) -> None:
+    """Test hook (pa_testing_set_wait_limit): the cycle limit of the decode
+    kernels' waits on other roles for later launches; 0 restores the default."""
+    _check(load_library().pa_testing_set_wait_limit(int(cycles)), "pa_testing_set_wait_limit")
 
 
 def pa_status_clear(workspace, stream=None) -> None:
@@ -510,23 +535,35 @@ class GraphStep:
         self.stream = torch.cuda.Stream(device=dev)
         self.graph = None
 
-    def _enqueue(self):
+    def _enqueue(self, events=None):
+        """Enqueue the step's stages on its stream; with ``events`` (five CUDA
+        events), record one before the host-to-device copy and one after each
+        stage (copy in, device planner, attention, copy out)."""
         import torch
         lib, cfg, s = load_library(), self.cfg, self.stream
+
+        def mark(k):
+            if events is not None:
+                events[k].record(s)
+        mark(0)
         with torch.cuda.stream(s):
             self.d_arena.copy_(self.h_arena, non_blocking=True)
+        mark(1)
         _check(lib.pa_plan_device(
             ctypes.byref(cfg), _tptr(self._dcl), _tptr(self._dql), _tptr(self.work),
             self.work_cap, _tptr(self.combine), self.comb_cap, _tptr(self.counts),
             _tptr(self.workspace), ctypes.c_void_p(s.cuda_stream)), "pa_plan_device")
+        mark(2)
         _check(lib.pa_forward_device_plan(
             ctypes.byref(cfg), _tptr(self._dq), _tptr(self.key_cache), _tptr(self.value_cache),
             _tptr(self._dbt), _tptr(self._dcl), _tptr(self._dql), _tptr(self.mask),
             _tptr(self.alibi_slopes), _tptr(self.work), self.work_cap, _tptr(self.combine),
             self.comb_cap, _tptr(self.counts), _tptr(self.workspace), self.workspace.numel(),
             _tptr(self.d_out), ctypes.c_void_p(s.cuda_stream)), "pa_forward_device_plan")
+        mark(3)
         with torch.cuda.stream(s):
             self.out.copy_(self.d_out, non_blocking=True)
+        mark(4)
 
     def record(self):
         """Run the step once directly (kernel attributes and tensor maps are set
@@ -538,6 +575,13 @@ class GraphStep:
         with torch.cuda.graph(g, stream=self.stream):
             self._enqueue()
         self.graph = g
+
+    def run_stages(self, events):
+        """Run the step's stages directly (no graph), recording ``events`` (five
+        CUDA events) around them for timing each stage, and wait."""
+        self._enqueue(events)
+        self.stream.synchronize()
+        return self.out
 
     def run(self):
         """Replay the step and wait for it; returns the pinned ``out`` tensor."""

@@ -5,10 +5,12 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
 #include "pa.h"
+#include "pa_testing.h"
 #include "pa_combine.cuh"
 #include "pa_decode_mma.cuh"
 #include "pa_decode_tc.cuh"
@@ -157,9 +159,61 @@ bool cache_map_3d(CUtensorMap* m, const void* base, const pa_config& c, int hs, 
   return cached_map(m, k, strides);
 }
 
+// The query [batch, H, hk] of a launch with one query token per sequence, as a
+// 3-D tensor for the tcgen05 kernel: dims (64 elements of a head-dim block,
+// batch * H rows, hk / 64 blocks), strides (row stride hk * 2 bytes, 128); a
+// box is G rows (the heads of one kv head, consecutive in memory) of one
+// 64-dim block, landing as [G][128 B] with the 128-byte swizzle.
+bool query_map(CUtensorMap* m, const void* query, const pa_config& c) {
+  MapKey k{};
+  k.base = query;
+  k.rank = 3;
+  k.swizzle = int(CU_TENSOR_MAP_SWIZZLE_128B);
+  k.dims[0] = 64;
+  k.dims[1] = uint64_t(c.batch) * c.num_heads;
+  k.dims[2] = uint64_t(c.head_size_k / 64);
+  k.box[0] = 64;
+  k.box[1] = uint32_t(c.num_heads / c.kv_heads);
+  k.box[2] = 1;
+  const cuuint64_t strides[2] = {cuuint64_t(c.head_size_k) * 2, 128};
+  return cached_map(m, k, strides);
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Cycle limit of the decode kernels' waits on other roles (0: the default);
+// set only through pa_testing_set_wait_limit.
+std::atomic<long long> g_wait_limit{0};
+
 }  // namespace
+
+pa_status check_forward(const pa_config* cfg, const void* query, const void* key_cache,
+                        const void* value_cache, const int32_t* block_tables,
+                        const int32_t* context_lens, const void* mask, const float* alibi_slopes,
+                        const int32_t* work, int64_t n_items, const int32_t* combine,
+                        int64_t n_combine, const void* workspace, size_t workspace_bytes,
+                        const void* out, bool check_workspace) {
+  pa_status st = validate_config(cfg);
+  if (st != PA_OK) return st;
+  const pa_config& c = *cfg;
+  if (!query || !key_cache || !value_cache || !block_tables || !context_lens || !out ||
+      (check_workspace && !workspace))
+    return PA_ERR_INVALID_ARG;
+  const bool has_mask = c.mask_type == PA_MASK_NORM_COMPRESS || c.mask_type == PA_MASK_NORM;
+  if (has_mask != (mask != nullptr)) return PA_ERR_INVALID_ARG;
+  if ((c.mask_type == PA_MASK_ALIBI) != (alibi_slopes != nullptr)) return PA_ERR_INVALID_ARG;
+  if (n_items < 0 || n_combine < 0 || n_items > INT32_MAX || n_combine > INT32_MAX)
+    return PA_ERR_INVALID_ARG;
+  if ((n_items > 0 && !work) || (n_combine > 0 && !combine)) return PA_ERR_INVALID_ARG;
+  // value_cache == key_cache: the shared-KV layout, V = first hv dims of each K row
+  if (value_cache == key_cache && c.head_size_v > c.head_size_k) return PA_ERR_INVALID_ARG;
+  if (!aligned(query, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+      !aligned(out, 16) || (check_workspace && !aligned(workspace, 256)))
+    return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < PA_STATUS_BYTES) return PA_ERR_BUFFER_TOO_SMALL;
+  return PA_OK;
+}
+
 }  // namespace pa
 
 namespace {
@@ -175,25 +229,12 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
                        const int32_t* combine, int64_t n_combine, const int32_t* counts,
                        void* workspace, size_t workspace_bytes, void* out, void* stream_) {
   using namespace pa;
-  pa_status st = validate_config(cfg);
+  const pa_status st = check_forward(cfg, query, key_cache, value_cache, block_tables,
+                                     context_lens, mask, alibi_slopes, work, n_items, combine,
+                                     n_combine, workspace, workspace_bytes, out, true);
   if (st != PA_OK) return st;
   const pa_config& c = *cfg;
-  if (!query || !key_cache || !value_cache || !block_tables || !context_lens || !out ||
-      !workspace)
-    return PA_ERR_INVALID_ARG;
-  const bool has_mask = c.mask_type == PA_MASK_NORM_COMPRESS || c.mask_type == PA_MASK_NORM;
-  if (has_mask != (mask != nullptr)) return PA_ERR_INVALID_ARG;
-  if ((c.mask_type == PA_MASK_ALIBI) != (alibi_slopes != nullptr)) return PA_ERR_INVALID_ARG;
-  if (n_items < 0 || n_combine < 0 || n_items > INT32_MAX || n_combine > INT32_MAX)
-    return PA_ERR_INVALID_ARG;
-  if ((n_items > 0 && !work) || (n_combine > 0 && !combine)) return PA_ERR_INVALID_ARG;
-  // value_cache == key_cache: the shared-KV layout, V = first hv dims of each K row
   const bool kv_shared = value_cache == key_cache;
-  if (kv_shared && c.head_size_v > c.head_size_k) return PA_ERR_INVALID_ARG;
-  if (!aligned(query, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
-      !aligned(out, 16) || !aligned(workspace, 256))
-    return PA_ERR_INVALID_ARG;
-  if (workspace_bytes < PA_STATUS_BYTES) return PA_ERR_BUFFER_TOO_SMALL;
   if (n_items == 0) return PA_OK;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
@@ -230,6 +271,8 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
   P.mask_kv = int64_t(c.max_blocks_per_seq) * c.block_size;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / std::sqrt(float(hk));
   P.scale_log2 = scale * kLog2e;
+  const long long wlim = g_wait_limit.load(std::memory_order_relaxed);
+  P.wait_limit = wlim > 0 ? wlim : kWaitLimitCycles;
 
   cudaError_t err;
   if (TR <= PA_FMA_MAX_ROWS) {
@@ -268,11 +311,20 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
     if (!tc_supported(hk, hv)) return PA_ERR_UNSUPPORTED;
     const int rows = c.block_size < 64 ? c.block_size : 64;
     const int halves = rows == 64 ? 2 : 1;
-    CUtensorMap tmk, tmv;
+    CUtensorMap tmk, tmv, tmq;
     if (!cache_map_3d(&tmk, key_cache, c, hk, rows, halves) ||
         !cache_map_3d(&tmv, value_cache, c, kv_shared ? hk : hv, rows, halves))
       return PA_ERR_CUDA;
-    err = launch_tc(tmk, tmv, P, n_items, stream);
+    // One query token per sequence (decode): a tile's rows are the G heads of
+    // one kv head, consecutive in the query, so the producer fetches the tile
+    // with TMA ahead of the K ring. Otherwise the softmax warps load it.
+    P.q_tma = 0;
+    tmq = tmk;
+    if (max_q(c) == 1) {
+      if (!query_map(&tmq, query, c)) return PA_ERR_CUDA;
+      P.q_tma = 1;
+    }
+    err = launch_tc(tmk, tmv, tmq, P, n_items, stream);
   }
   if (err != cudaSuccess) return PA_ERR_CUDA;
   if (n_combine > 0) {
@@ -396,6 +448,12 @@ extern "C" pa_status pa_status_read(const void* workspace, void* stream_, uint32
   if (v & PA_STATUS_BIT_BLOCK_INDEX) return PA_ERR_BLOCK_INDEX;
   if (v & PA_STATUS_BIT_WORKSPACE) return PA_ERR_BUFFER_TOO_SMALL;
   if (v & PA_STATUS_BIT_PLAN) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+extern "C" pa_status pa_testing_set_wait_limit(long long cycles) {
+  if (cycles < 0) return PA_ERR_INVALID_ARG;
+  pa::g_wait_limit.store(cycles, std::memory_order_relaxed);
   return PA_OK;
 }
 

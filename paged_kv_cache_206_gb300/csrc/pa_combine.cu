@@ -1,5 +1,5 @@
-// Split-KV reduction: the FlashDecode reduction tasks of
-// SparseAttnSharedkvMetadata (`metadata`: "每个vector核上FlashDecode的规约任务"),
+// Split-KV reduction (SparseAttnSharedkvMetadata, 参数说明, the `metadata`
+// output, whose list also carries the per-core FlashDecode merge tasks),
 // restated for one GPU. Each split s of a query tile left a normalised partial
 // output O_s and its log-sum-exp lse_s; the merged row is
 //   out = sum_s exp(lse_s - M) * O_s / sum_s exp(lse_s - M),  M = max_s lse_s.
@@ -11,7 +11,7 @@
 namespace pa {
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams C) {
-  __shared__ float wts[kCombineThreads / 32][kCombineMaxSplits];
+  constexpr int kBatch = 16;  // splits whose partial rows a lane has in flight at once
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (C.counts && int(blockIdx.x) >= C.counts[1]) return;
   // Launched as a programmatic dependent of the attention kernel: wait until
@@ -29,35 +29,54 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   const int rr = blockIdx.y * (kCombineThreads / 32) + warp;
   if (rr >= nrows) return;
   const float* lse = C.part_lse + slot0 + rr;  // split s at lse[s * nrows]
+  // this warp's 128 dims (blockIdx.z), 4 a lane; split s at po[s * split_stride]
+  const int d = blockIdx.z * 128 + lane * 4;
+  const bool active = d < C.hv;
+  const int64_t split_stride = int64_t(nrows) * C.hv;
+  const float* po = C.part_o + (int64_t(slot0) + rr) * C.hv + d;
+  // The first batch of partial rows is loaded together with the LSEs: one
+  // round trip to L2 before the arithmetic, not one per pass.
+  float4 v[kBatch];
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k)
+    v[k] = (k < S && active) ? __ldg(reinterpret_cast<const float4*>(po + k * split_stride))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
   float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, lse[int64_t(s) * nrows]);
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldg(lse + int64_t(s) * nrows));
+#pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float den = 0.f;
+  float den = 0.f, w_lane = 0.f;  // lane s < 32 keeps split s's weight
   for (int s = lane; s < S; s += 32) {
-    const float w = __expf(lse[int64_t(s) * nrows] - M);
-    if (s < kCombineMaxSplits) wts[warp][s] = w;
+    const float w = __expf(__ldg(lse + int64_t(s) * nrows) - M);
+    if (s < 32) w_lane = w;
     den += w;
   }
+#pragma unroll
   for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  __syncwarp();
-  const float inv = 1.f / den;
-  const int r = r0 + rr, i = r / C.group, h = kvh * C.group + r % C.group;
-  __half* dst = C.out + (int64_t(q_start + i) * C.num_heads + h) * C.hv;
-  const float* po = C.part_o + (int64_t(slot0) + rr) * C.hv;
-  const int64_t split_stride = int64_t(nrows) * C.hv;
-  // this warp's 128 dims (blockIdx.z); loads of several splits in flight at once
-  const int d = blockIdx.z * 128 + lane * 4;
-  if (d < C.hv) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int s = 0; s < S; ++s) {
-      const float w = s < kCombineMaxSplits ? wts[warp][s] : __expf(lse[int64_t(s) * nrows] - M);
-      const float4 v = __ldg(reinterpret_cast<const float4*>(po + s * split_stride + d));
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < S; s0 += kBatch) {
+    if (s0 > 0) {
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (s0 + k < S && active)
+          v[k] = __ldg(reinterpret_cast<const float4*>(po + (s0 + k) * split_stride));
     }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int s = s0 + k;
+      if (s >= S) break;
+      const float w = s < 32 ? __shfl_sync(0xffffffffu, w_lane, s)
+                             : __expf(__ldg(lse + int64_t(s) * nrows) - M);
+      acc.x += w * v[k].x;
+      acc.y += w * v[k].y;
+      acc.z += w * v[k].z;
+      acc.w += w * v[k].w;
+    }
+  }
+  if (active) {
+    const float inv = 1.f / den;
+    const int r = r0 + rr, i = r / C.group, h = kvh * C.group + r % C.group;
+    __half* dst = C.out + (int64_t(q_start + i) * C.num_heads + h) * C.hv;
     __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
     __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
     uint2 pk;

@@ -10,7 +10,6 @@
 namespace pa {
 
 constexpr int kCombineThreads = 256;     // 8 warps, one row each
-constexpr int kCombineMaxSplits = 512;   // weights cached in shared memory
 
 struct CombineParams {
   const int32_t* combine;

@@ -7,8 +7,10 @@
 // The KV range of a work item is cut into 64-token tiles. One CTA per item,
 // 12 warps:
 //   warp 0     K producer: 3-D TMA boxes of 64 tokens x 128 dims (16 KB, two
-//              128-byte-swizzled 64-dim halves) into a 3-slot K ring.
-//   warp 10    V producer: the same for V into a 5-slot V ring.
+//              128-byte-swizzled 64-dim halves) into the K ring.
+//   warp 10    V producer: the same for V into the V ring (ring sizes: TcCfg,
+//              from the shared memory the query tile leaves, e.g. 5 K + 4 V
+//              slots at 512 dims and 64 rows).
 //   warp 1     allocates TMEM; one thread issues S^T[64 tok x 64 rows] = K . Q^T
 //              (M=64; A, B K-major) into one of two S^T buffers in TMEM, up to
 //              two tiles ahead of the softmax.
@@ -22,9 +24,9 @@
 //              practice the first tile; O^T and the sums are rescaled then
 //              (exact: the final normalisation uses the same reference). Row
 //              sums accumulate per token and are reduced across tokens once, at
-//              the end. P^T (fp16, double-buffered) goes to shared memory in the
-//              MN-major swizzled layout the PV MMA reads. Epilogue: thread =
-//              output dim, O^T / l from TMEM to the output or the split partials.
+//              the end. P^T (fp16) goes to shared memory in the MN-major
+//              swizzled layout the PV MMA reads. Epilogue: thread = output dim,
+//              O^T / l from TMEM to the output or the split partials.
 // Separate rings and issuers keep K streaming into QK while a tile's V waits
 // for its softmax. Every wait is bounded; on a timeout the CTA records
 // PA_STATUS_BIT_TIMEOUT, lets its copies land, frees its TMEM and exits.
@@ -240,9 +242,10 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // Lane 0 waits; the whole warp gets its verdict.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane,
+                                          long long limit = kWaitLimitCycles) {
   bool ok = true;
-  if (lane == 0) ok = mbar_wait(bar, parity);
+  if (lane == 0) ok = mbar_wait(bar, parity, limit);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
@@ -256,7 +259,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <int HK, int HV, int NR, bool SH>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-    const FwdParams P) {
+    const __grid_constant__ CUtensorMap tmq, const FwdParams P) {
   constexpr int KH = HK / 64;         // 64-dim halves of a K row
   constexpr int KS = (KH + 1) / 2;    // K slots per tile (128 dims each; the
                                       // last holds one half when KH is odd)
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     }
     mbar_init(qk_done, 1);
     mbar_init(o_done, 1);
-    mbar_init(q_ready, 8);
+    mbar_init(q_ready, P.q_tma ? 9 : 8);  // + the producer's query copy
     fence_barrier_init();
     flags[1] = 0;
   }
@@ -369,6 +372,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       // 64-dim blocks per kv head in the map's rows: a shared-KV V map spans the K rows
       const int zbase = it.kvh * ((is_k || P.kv_shared ? HK : HV) / 64);
       const uint64_t pol = policy_evict_first();
+      if (is_k && P.q_tma) {
+        // The query tile first, ahead of the K ring in the same queue: its G
+        // rows (heads kvh * G .. of the sequence's one query token) are
+        // consecutive in the query; one box per 64-dim block, landing where
+        // the QK MMA reads it. Every split of the tile reads the same tile,
+        // so keep it in L2.
+        const int G = P.group;
+        mbar_arrive_expect_tx(q_ready, uint32_t(KH) * G * 128);
+        const int row0 = it.q_start * P.num_heads + it.kvh * G;
+        for (int blk = 0; blk < KH; ++blk)
+          tma_load_3d(q_s + blk * (NR * 128), &tmq, q_ready, 0, row0, blk, policy_evict_last());
+      }
       const int32_t* bt_row = P.block_tables + int64_t(it.b) * P.max_blocks_per_seq;
       const int box_rows = bs < kTcTok ? bs : kTcTok;
       const int pieces = kTcTok / box_rows;
@@ -401,7 +416,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
           const bool one_half = is_k && (KH & 1) && sl == KS - 1 && box_rows != kTcTok;
           const uint32_t bytes = uint32_t(npieces) * box_rows * (one_half ? 128 : 256);
           const int slot = issued % nslots;
-          if (!mbar_wait(&empty[slot], ((issued / nslots) & 1) ^ 1)) {
+          if (!mbar_wait(&empty[slot], ((issued / nslots) & 1) ^ 1, P.wait_limit)) {
             ok = false;
             break;
           }
@@ -429,9 +444,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         }
       }
       if (!ok) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
-      // let every issued copy land before the CTA can exit (bounded waits)
+      // let every issued copy land before the CTA can exit (bounded waits,
+      // default limit), the query tile's too
       for (int i = issued - nslots > 0 ? issued - nslots : 0; i < issued; ++i)
         mbar_wait(&full[i % nslots], (i / nslots) & 1);
+      if (is_k && P.q_tma) mbar_wait(q_ready, 0);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -441,13 +458,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const uint32_t q_addr = smem_u32(q_s), ring_addr = smem_u32(kring);
     int consumed = 0;
     // the softmax warps load the query tile while the producers already stream
-    if (ntiles > 0 && !warp_wait(q_ready, 0, lane)) ok = false;
+    if (ntiles > 0 && !warp_wait(q_ready, 0, lane, P.wait_limit)) ok = false;
     for (int m = 0; m < ntiles && ok; ++m) {
-      if (m >= 2 && !warp_wait(&s_free[m & 1], ((m >> 1) - 1) & 1, lane)) { ok = false; break; }
+      if (m >= 2 && !warp_wait(&s_free[m & 1], ((m >> 1) - 1) & 1, lane, P.wait_limit)) { ok = false; break; }
       tc_fence_after();
       for (int ks = 0; ks < KS; ++ks, ++consumed) {
         const int slot = consumed % kKSlots;
-        if (!warp_wait(&kfull[slot], (consumed / kKSlots) & 1, lane)) { ok = false; break; }
+        if (!warp_wait(&kfull[slot], (consumed / kKSlots) & 1, lane, P.wait_limit)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
@@ -479,7 +496,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     int consumed = 0;
     for (int n = 0; n < ntiles && ok; ++n) {
       const int pb = n % kTcPBufs;
-      if (!warp_wait(&p_full[pb], (n / kTcPBufs) & 1, lane)) { ok = false; break; }
+      if (!warp_wait(&p_full[pb], (n / kTcPBufs) & 1, lane, P.wait_limit)) { ok = false; break; }
       tc_fence_after();
       const int nvalid = min(kTcTok, it.tok1 - (it.tok0 + n * kTcTok));
       for (int oc = 0; oc < VS; ++oc, ++consumed) {
@@ -488,7 +505,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         const int ring_slots = SH ? kKSlots : kVSlots;
         const int seq = SH ? n * KS + oc : consumed;
         const int slot = seq % ring_slots;
-        if (!warp_wait(SH ? &kfull[slot] : &vfull[slot], (seq / ring_slots) & 1, lane)) { ok = false; break; }
+        if (!warp_wait(SH ? &kfull[slot] : &vfull[slot], (seq / ring_slots) & 1, lane, P.wait_limit)) { ok = false; break; }
         if (nvalid < kTcTok) {
           // V rows of tokens past the range may hold anything (NaN included):
           // zero them (both 64-dim halves) so that p = 0 contributes nothing.
@@ -526,32 +543,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     // ================= softmax warps 2-9 =================
     // Query tile first (the producers are already streaming K and V): row r
     // of the tile, chunk c (8 dims) -> box c/8, swizzled position, in two
-    // rounds whose loads are all issued before their stores.
+    // rounds whose loads are all issued before their stores. With the query
+    // by TMA (P.q_tma) the producer fetches rows 0..G-1 and these warps only
+    // zero the rows past them.
     {
       const int st = tid - 64;  // 0..255
-      constexpr int kChunks = NR * (HK / 8);
-      constexpr int kPer = (kChunks + 255) / 256;
-      constexpr int kHalf = (kPer + 1) / 2;
+      if (P.q_tma) {
+        const int G = P.group;
+        const int pad = (NR - G) * 8;  // 16-byte chunks per 64-dim block past row G
+        for (int i = st; i < (HK / 64) * pad; i += 256)
+          *reinterpret_cast<uint4*>(q_s + (i / pad) * (NR * 128) + G * 128 + (i % pad) * 16) =
+              make_uint4(0, 0, 0, 0);
+      } else {
+        constexpr int kChunks = NR * (HK / 8);
+        constexpr int kPer = (kChunks + 255) / 256;
+        constexpr int kHalf = (kPer + 1) / 2;
 #pragma unroll
-      for (int round = 0; round < 2; ++round) {
-        uint4 v[kHalf];
+        for (int round = 0; round < 2; ++round) {
+          uint4 v[kHalf];
 #pragma unroll
-        for (int k = 0; k < kHalf; ++k) {
-          const int idx = st + (round * kHalf + k) * 256;
-          const int r = idx / (HK / 8), c = idx % (HK / 8);
-          v[k] = make_uint4(0, 0, 0, 0);
-          if (round * kHalf + k < kPer && idx < kChunks && r < it.nrows) {
-            const int rr = it.r0 + r;
-            v[k] = *reinterpret_cast<const uint4*>(
-                P.query + (int64_t(it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G) * HK + c * 8);
+          for (int k = 0; k < kHalf; ++k) {
+            const int idx = st + (round * kHalf + k) * 256;
+            const int r = idx / (HK / 8), c = idx % (HK / 8);
+            v[k] = make_uint4(0, 0, 0, 0);
+            if (round * kHalf + k < kPer && idx < kChunks && r < it.nrows) {
+              const int rr = it.r0 + r;
+              v[k] = *reinterpret_cast<const uint4*>(
+                  P.query + (int64_t(it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G) * HK + c * 8);
+            }
           }
-        }
 #pragma unroll
-        for (int k = 0; k < kHalf; ++k) {
-          const int idx = st + (round * kHalf + k) * 256;
-          const int r = idx / (HK / 8), c = idx % (HK / 8);
-          if (round * kHalf + k < kPer && idx < kChunks)
-            *reinterpret_cast<uint4*>(q_s + (c >> 3) * (NR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v[k];
+          for (int k = 0; k < kHalf; ++k) {
+            const int idx = st + (round * kHalf + k) * 256;
+            const int r = idx / (HK / 8), c = idx % (HK / 8);
+            if (round * kHalf + k < kPer && idx < kChunks)
+              *reinterpret_cast<uint4*>(q_s + (c >> 3) * (NR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v[k];
+          }
         }
       }
       if (NR < kTcRows)  // P^T columns past NR are read by the PV MMA: keep them zero
@@ -575,7 +602,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const float4* m_used4 = reinterpret_cast<const float4*>(m_used + rbase);
     bool ok = true;
     for (int n = 0; n < ntiles; ++n) {
-      const bool got = mbar_wait(&s_full[n & 1], (n >> 1) & 1);
+      const bool got = mbar_wait(&s_full[n & 1], (n >> 1) & 1, P.wait_limit);
       if (softmax_bar_or(!got)) { ok = false; break; }  // all softmax warps agree
       tc_fence_after();
       float s[RH];
@@ -676,9 +703,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       {
         bool pv = true;
         if (grew && n >= 1)
-          pv = mbar_wait(&pv_done[(n - 1) % kTcPBufs], ((n - 1) / kTcPBufs) & 1);
+          pv = mbar_wait(&pv_done[(n - 1) % kTcPBufs], ((n - 1) / kTcPBufs) & 1, P.wait_limit);
         if (n >= kTcPBufs)
-          pv = pv && mbar_wait(&pv_done[n % kTcPBufs], ((n - kTcPBufs) / kTcPBufs) & 1);
+          pv = pv && mbar_wait(&pv_done[n % kTcPBufs], ((n - kTcPBufs) / kTcPBufs) & 1, P.wait_limit);
         if (softmax_bar_or(!pv)) { ok = false; break; }
         tc_fence_after();
       }
@@ -752,7 +779,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       }
     }
     launch_dependents();
-    const bool got = ok && mbar_wait(o_done, 0);
+    const bool got = ok && mbar_wait(o_done, 0, P.wait_limit);
     const bool done = !softmax_bar_or(!got);
     if (done && ntiles > 0) {
       tc_fence_after();
@@ -785,6 +812,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     }
   }
   // ---- teardown: every tcgen05 op has completed (o_done) before TMEM is freed
+  // (these two waits take the default limit whatever P.wait_limit is)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -801,8 +829,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
 
 // Launch with NR rows per tile (instantiated in pa_decode_tc.cu, _n16.cu, _n32.cu).
 template <int NR>
-cudaError_t launch_tc_rows(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdParams& P,
-                           int64_t n_items, cudaStream_t stream);
+cudaError_t launch_tc_rows(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
+                           const FwdParams& P, int64_t n_items, cudaStream_t stream);
 
 // Rows per tile of a launch: the group's rows G * max_q rounded up to 16, 32 or 64.
 inline int tc_tile_rows(int group, int max_q) {
@@ -810,18 +838,21 @@ inline int tc_tile_rows(int group, int max_q) {
   return r <= 16 ? 16 : (r <= 32 ? 32 : 64);
 }
 
-cudaError_t launch_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdParams& P,
-                      int64_t n_items, cudaStream_t stream);
+// tmq: the query as the tiles' TMA source when P.q_tma is set (one query
+// token per sequence), else unused.
+cudaError_t launch_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
+                      const FwdParams& P, int64_t n_items, cudaStream_t stream);
 
 // One launcher body for every NR: the head-size pairs of tc_supported.
 template <int NR>
 cudaError_t launch_tc_rows_impl(const CUtensorMap& tmk, const CUtensorMap& tmv,
-                                const FwdParams& P, int64_t n_items, cudaStream_t stream,
+                                const CUtensorMap& tmq, const FwdParams& P, int64_t n_items,
+                                cudaStream_t stream,
                                 cudaError_t (*set_attr)(const void*, int)) {
   auto go = [&](auto kern, uint32_t bytes) -> cudaError_t {
     cudaError_t e = set_attr(reinterpret_cast<const void*>(kern), int(bytes));
     if (e != cudaSuccess) return e;
-    kern<<<unsigned(n_items), kTcThreads, bytes, stream>>>(tmk, tmv, P);
+    kern<<<unsigned(n_items), kTcThreads, bytes, stream>>>(tmk, tmv, tmq, P);
     return cudaGetLastError();
   };
   const bool sh = P.kv_shared != 0;

@@ -5,9 +5,10 @@
 namespace pa {
 
 template <>
-cudaError_t launch_tc_rows<32>(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdParams& P,
-                               int64_t n_items, cudaStream_t stream) {
-  return launch_tc_rows_impl<32>(tmk, tmv, P, n_items, stream, ensure_smem_attr);
+cudaError_t launch_tc_rows<32>(const CUtensorMap& tmk, const CUtensorMap& tmv,
+                               const CUtensorMap& tmq, const FwdParams& P, int64_t n_items,
+                               cudaStream_t stream) {
+  return launch_tc_rows_impl<32>(tmk, tmv, tmq, P, n_items, stream, ensure_smem_attr);
 }
 
 }  // namespace pa

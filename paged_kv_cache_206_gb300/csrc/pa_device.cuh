@@ -11,7 +11,11 @@
 namespace pa {
 
 // A wait on an mbarrier gives up after this many SM clock cycles (about two
-// seconds at GB300 clocks); a legitimate wait is microseconds.
+// seconds at GB300 clocks); a legitimate wait is microseconds. The decode
+// kernels take the limit of their waits from FwdParams::wait_limit (this value
+// unless a test lowers it); a wait for a CTA's own copies or tensor-core
+// operations to finish before it exits (the drains and the teardown) always
+// uses this one.
 constexpr long long kWaitLimitCycles = 4ll << 30;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -42,6 +46,8 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One poll of the phase with the given parity (the thread may be suspended
+// inside it for a system-dependent time).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -54,15 +60,48 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test without suspending the thread (returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete. Returns false
-// when the wait ran out of time.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// when the wait ran out of time (more than `limit` SM clock cycles). Each poll
+// (try_wait) may suspend the thread for a system-dependent time, so a limit
+// far below that time does not make a wait run out: the wait returns as soon
+// as its phase completes within the suspension.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
+}
+
+// mbar_wait for the warp-pipelined kernels, whose waits are only on their own
+// copies: under a lowered limit (tests) the polls do not suspend (test_wait),
+// so that the limit, not the suspension, decides. The tcgen05 kernels keep
+// mbar_wait: a second polling loop in their waits measured 7-10% slower, and
+// their waits on other roles run out under a lowered limit as they are.
+__device__ __forceinline__ bool mbar_wait_own(uint64_t* bar, uint32_t parity, long long limit) {
+  if (limit < kWaitLimitCycles) {
+    const long long t0 = clock64();
+    while (!mbar_test_wait(bar, parity)) {
+      if (clock64() - t0 > limit) return false;
+    }
+    return true;
+  }
+  return mbar_wait(bar, parity, limit);
 }
 
 // 2-D tiled TMA load of one box into shared memory, completing on `bar`.
@@ -176,9 +215,11 @@ struct FwdParams {
   int num_heads, kv_heads, group, hk, hv, block_size, max_blocks_per_seq, num_blocks;
   int mask_type;
   int kv_shared;     // V of a token = the first hv dims of its K row (value_cache == key_cache)
+  int q_tma;         // tcgen05 decode kernel: the query tile comes by TMA (tmq)
   int mask_q;        // PA_MASK_NORM: mask is [batch][mask_q][mask_kv]
   int64_t mask_kv;
   float scale_log2;  // scale * log2(e)
+  long long wait_limit;  // cycles a wait on another role's progress may take
 };
 
 // Bias (base 2) of a PA_MASK_NORM mask for query token i of sequence b and key j.

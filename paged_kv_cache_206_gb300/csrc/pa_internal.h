@@ -17,6 +17,16 @@ pa_status validate_config(const pa_config* cfg);
 
 inline int64_t max_q(const pa_config& c) { return c.max_seqlen_q > 0 ? c.max_seqlen_q : 1; }
 
+// The host-side checks of pa_forward (configuration, pointers, alignment,
+// workspace size), done before anything is enqueued; the workspace pointer
+// itself is checked (non-null, 256-byte aligned) only with check_workspace.
+pa_status check_forward(const pa_config* cfg, const void* query, const void* key_cache,
+                        const void* value_cache, const int32_t* block_tables,
+                        const int32_t* context_lens, const void* mask, const float* alibi_slopes,
+                        const int32_t* work, int64_t n_items, const int32_t* combine,
+                        int64_t n_combine, const void* workspace, size_t workspace_bytes,
+                        const void* out, bool check_workspace);
+
 // Tile height of a launch: every row of a (b, kv head) pair in one CTA when
 // the group is small enough for the CUDA-core kernel; for 64/128-dim heads
 // with more than 64 rows, 128-row tiles, or 256 (two 128-row query tiles
@@ -54,6 +64,7 @@ struct WorkspaceLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// [status][partial O][partial LSE], each part on a 256-byte boundary.
 inline WorkspaceLayout workspace_layout(int64_t partial_rows, int hv) {
   WorkspaceLayout w;
   w.partial_o = PA_STATUS_BYTES;

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "pa.h"
+#include "pa_internal.h"
 
 namespace {
 
@@ -50,8 +51,14 @@ extern "C" pa_status pa_forward_noalloc(const pa_config* cfg, const void* query,
                                         uint32_t* status, void* out, void* stream_) {
   if (workspace_bytes > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_BUFFER_TOO_SMALL;
   if (workspace_bytes < PA_STATUS_BYTES) workspace_bytes = PA_STATUS_BYTES;
+  // pa_forward's own host checks first, so that a rejected call enqueues
+  // nothing (the array is 256-byte aligned by its declaration)
+  pa_status st = pa::check_forward(cfg, query, key_cache, value_cache, block_tables, context_lens,
+                                   mask, alibi_slopes, work, n_items, combine, n_combine, nullptr,
+                                   workspace_bytes, out, false);
+  if (st != PA_OK) return st;
   void* scratch = nullptr;
-  pa_status st = scratch_on_current_device(&scratch);
+  st = scratch_on_current_device(&scratch);
   if (st != PA_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   // The array keeps the previous call's contents: the status word must start at 0.

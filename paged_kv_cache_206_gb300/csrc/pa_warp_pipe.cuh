@@ -87,6 +87,7 @@ struct WarpPipe {
   int kb0, kb1, warp, nw, lane, bs, hk, hv, kvh, num_blocks, nkbox, nvbox;
   bool shared;  // V is read from the K boxes (shared-KV cache): no V copies
   uint32_t* status;
+  long long wait_limit;
   uint64_t pol;
   const CUtensorMap* tmk;
   const CUtensorMap* tmv;
@@ -113,6 +114,7 @@ struct WarpPipe {
     kb1 = it.kb1;
     num_blocks = P.num_blocks;
     status = P.status;
+    wait_limit = P.wait_limit;
     tmk = k_map;
     tmv = v_map;
     pol = policy_evict_first();
@@ -165,8 +167,12 @@ struct WarpPipe {
     }
   }
 
-  // Bounded wait for the n-th sub-tile (any thread).
-  __device__ __forceinline__ bool wait(int n) { return mbar_wait(&bars[n % NBUF], (n / NBUF) & 1); }
+  // Bounded wait for the n-th sub-tile, warp-collective: every lane waits
+  // (each lane then reads the buffer), and the verdict is the warp's, so that
+  // a lane whose wait ran out and one whose copy landed meanwhile cannot part.
+  __device__ __forceinline__ bool wait(int n) {
+    return __all_sync(0xffffffffu, mbar_wait_own(&bars[n % NBUF], (n / NBUF) & 1, wait_limit));
+  }
 
   // Called by the warp once it is done reading buffer n % NBUF.
   __device__ __forceinline__ void release_and_refill(int n, int nmine) {
@@ -176,10 +182,14 @@ struct WarpPipe {
   }
 
   // After a timed-out wait at sub-tile `failed`: let the copies still in
-  // flight land (bounded waits) before the CTA's shared memory is released.
+  // flight (sub-tiles failed .. failed + NBUF - 1, the ones issued and not yet
+  // consumed) land before the CTA's shared memory is released. These waits
+  // take the default limit whatever wait_limit is: the copies were issued and
+  // land within microseconds.
   __device__ __forceinline__ void drain(int failed, int nmine) {
     if (lane == 0) set_status(status, PA_STATUS_BIT_TIMEOUT);
-    for (int m = failed; m < failed + NBUF && m < nmine; ++m) wait(m);
+    for (int m = failed; m < failed + NBUF && m < nmine; ++m)
+      mbar_wait(&bars[m % NBUF], (m / NBUF) & 1);
   }
 };
 

@@ -139,3 +139,58 @@ def test_plan_bounds_and_device_plan_host_checks(lib):
                                       None, fake, 4, None, 0, None, fake, 256, fake,
                                       None) == pa.PA_ERR_INVALID_ARG  # counts required
     assert lib.pa_status_read(None, None, None) == pa.PA_ERR_INVALID_ARG
+
+
+def _header_define(name):
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    m = re.search(r"^#define\s+" + name + r"\s+(.+)$", text, re.M)
+    assert m, name
+    expr = re.sub(r"/\*.*?\*/", "", m.group(1)).strip()
+    expr = re.sub(r"(\d+)u\b", r"\1", expr)  # C unsigned suffixes
+    assert re.fullmatch(r"[0-9()<< +*x]+", expr), expr
+    return int(eval(expr))
+
+
+def test_binding_constants_match_the_header():
+    """The binding restates some of pa.h's #defines; they must agree."""
+    for name in ("PA_NOALLOC_SCRATCH_BYTES", "PA_STATUS_BYTES", "PA_WORK_INTS",
+                 "PA_COMBINE_INTS", "PA_FMA_MAX_ROWS", "PA_TC_TILE_ROWS", "PA_PF_TILE_ROWS",
+                 "PA_PF_PAIR_ROWS", "PA_PLAN_COUNTS", "PA_STATUS_BIT_BLOCK_INDEX",
+                 "PA_STATUS_BIT_TIMEOUT", "PA_STATUS_BIT_WORKSPACE", "PA_STATUS_BIT_PLAN"):
+        assert getattr(pa, name) == _header_define(name), name
+
+
+def test_probe_and_testing_hook_host_checks(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    probe = lib.pa_hbm_read_probe
+    assert probe(None, 1024, 1, fake, None) == pa.PA_ERR_INVALID_ARG
+    assert probe(fake, 0, 1, fake, None) == pa.PA_ERR_INVALID_ARG
+    assert probe(fake, 1000, 1, fake, None) == pa.PA_ERR_INVALID_ARG       # not a multiple of 32
+    assert probe(ctypes.c_void_p((1 << 20) + 16), 1024, 1, fake, None) == pa.PA_ERR_INVALID_ARG
+    assert probe(fake, 1024, 0, fake, None) == pa.PA_ERR_INVALID_ARG
+    assert probe(fake, 1024, 9, fake, None) == pa.PA_ERR_INVALID_ARG
+    assert probe(fake, 1024, 1, None, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_testing_set_wait_limit(-1) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_testing_set_wait_limit(0) == pa.PA_OK
+
+
+def test_noalloc_rejects_bad_arguments_before_enqueueing(lib):
+    """pa_forward_noalloc runs pa_forward's host checks before it touches the
+    stream: with no CUDA device, a call that passed them would fail in the
+    CUDA runtime instead (PA_ERR_CUDA), so every bad call here must come back
+    PA_ERR_INVALID_ARG."""
+    c = _cfg()
+    fake = ctypes.c_void_p(1 << 20)
+
+    def call(**kw):
+        a = dict(query=fake, key=fake, value=fake, bt=fake, ctx=fake, mask=None, slopes=None,
+                 work=fake, n_items=1, ws_bytes=256, out=fake)
+        a.update(kw)
+        return lib.pa_forward_noalloc(ctypes.byref(c), a["query"], a["key"], a["value"], a["bt"],
+                                      a["ctx"], None, a["mask"], a["slopes"], a["work"],
+                                      a["n_items"], None, 0, a["ws_bytes"], None, a["out"], None)
+    assert call(query=None) == pa.PA_ERR_INVALID_ARG
+    assert call(out=ctypes.c_void_p((1 << 20) + 2)) == pa.PA_ERR_INVALID_ARG
+    assert call(mask=fake) == pa.PA_ERR_INVALID_ARG
+    assert call(work=None) == pa.PA_ERR_INVALID_ARG
+    assert call(ws_bytes=pa.PA_NOALLOC_SCRATCH_BYTES + 1) == pa.PA_ERR_BUFFER_TOO_SMALL

@@ -37,13 +37,14 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def call_noalloc(db, out, status, workspace_bytes=None):
+def call_noalloc(db, out, status, workspace_bytes=None, block_tables=None):
     """The C ABI call itself (through ctypes), on the current stream."""
     lib = pa.load_library()
     n_comb = 0 if db.combine is None else db.combine.shape[0]
+    bt = db.block_tables if block_tables is None else block_tables
     return lib.pa_forward_noalloc(
         ctypes.byref(db.cfg), _ptr(db.query), _ptr(db.key_cache), _ptr(db.value_cache),
-        _ptr(db.block_tables), _ptr(db.context_lens), _ptr(db.q_seqlens), _ptr(db.mask),
+        _ptr(bt), _ptr(db.context_lens), _ptr(db.q_seqlens), _ptr(db.mask),
         _ptr(db.alibi_slopes), _ptr(db.work), db.work.shape[0], _ptr(db.combine), n_comb,
         db.plan.workspace_bytes if workspace_bytes is None else workspace_bytes, _ptr(status),
         _ptr(out), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
@@ -90,3 +91,28 @@ def test_noalloc_rejects_workspace_beyond_its_array():
     out = torch.empty_like(db.out)
     st = call_noalloc(db, out, None, workspace_bytes=pa.PA_NOALLOC_SCRATCH_BYTES + 1)
     assert st == pa.PA_ERR_BUFFER_TOO_SMALL
+
+
+def test_noalloc_status_reaches_the_caller_and_is_cleared_per_call():
+    """Each call starts from a cleared status word in the shared array, and a
+    kernel's status bit reaches the caller's `status`. The fault is made on the
+    host: one block-table entry past num_blocks, which the kernel flags and
+    never dereferences. The next clean call must report 0 again."""
+    w = W.gqa_decode(batch=4, max_len=600, seed=44)
+    db = pa.DeviceBatch(w, chunk_blocks=2)
+    assert db.combine is not None
+    bad = db.block_tables.clone()
+    bad[2, 0] = w.num_blocks + 5
+    status = torch.zeros(1, dtype=torch.int32, device=db.out.device)
+    out = torch.empty_like(db.out)
+    assert call_noalloc(db, out, status, block_tables=bad) == pa.PA_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) & pa.PA_STATUS_BIT_BLOCK_INDEX
+    status.fill_(-1)
+    assert call_noalloc(db, out, status) == pa.PA_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = db.forward()
+    assert db.status()[0] == pa.PA_OK
+    err = (out.double() - ref.double()).abs()
+    assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS
