@@ -377,6 +377,7 @@ def read_peak(dev, stream):
         if best is None or gbs > best["gbs"]:
             best = {"gbs": gbs, "ctas_per_sm": ctas, "ms": ms}
     del buf
+    torch.cuda.empty_cache()  # give the 2 GiB back before the workloads
     return {"value": best["gbs"], "unit": "GB/s", "bytes": READ_PROBE_BYTES,
             "ctas_per_sm": best["ctas_per_sm"],
             "how": "pa_hbm_read_probe: 256-bit loads (L1 bypassed, L2 evict-first), "
@@ -509,6 +510,7 @@ def measure(name, args, steps, dev, stream, flush, rank, peaks_, read_gbs, cpu_s
             "block_size": w.block_size, "q_per_seq": w.max_seqlen_q, "mask_type": w.mask_type,
             "shared_kv": w.shared_kv, "kv_bytes": kv_bytes, "qo_bytes": qo_bytes,
             "items": n_items, "combines": n_comb, "chunk_blocks": db.cfg.chunk_blocks,
+            "split_merge": "combine kernel" if n_comb else "none",
             "l2": "flushed before every step, outside the events: 512 MB written, then 256 MB "
                   "read back",
             "plan_us": plan_us},

@@ -45,9 +45,9 @@ def compare(got, ref):
 
 CASES = {
     # mma.sync kernel (4 rows: GQA 32/8), warp-pipelined TMA ring, split items
-    "warp_pipe_gqa": (lambda: W.gqa_decode(batch=6, max_len=1500, seed=60), 2),
+    "warp_pipe_gqa": (lambda: W.gqa_decode(batch=8, max_len=3000, seed=60), 2),
     # CUDA-core kernel (1 row), ALiBi
-    "warp_pipe_fma": (lambda: W.alibi_decode(batch=4, max_len=900, seed=61), 3),
+    "warp_pipe_fma": (lambda: W.alibi_decode(batch=16, max_len=2048, seed=61), 3),
     # tcgen05 kernel, 16 rows, 16-token blocks, split items
     "tc_r16_bs16": (lambda: W.make_workload("r16", context_lens=[100, 300, 17, 129],
                                             num_heads=16, kv_heads=1, head_size_k=128,
@@ -64,12 +64,22 @@ def test_short_wait_limit_times_out_and_the_context_survives(oracle_mod, name):
     make, chunk = CASES[name]
     w = make()
     db = pa.DeviceBatch(w, chunk_blocks=chunk)
-    pa.testing_set_wait_limit(32)
-    try:
-        db.forward()
-        st, bits = db.status()
-    finally:
-        pa.testing_set_wait_limit(0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=db.out.device)
+    # Whether a wait outlasts 32 cycles depends on when its copy lands: the
+    # L2 is flushed first so that the copies come from HBM, and the launch is
+    # tried up to three times; one report of a timeout is what is checked.
+    st, bits = pa.PA_OK, 0
+    for _ in range(3):
+        flush.zero_()
+        pa.testing_set_wait_limit(32)
+        try:
+            db.forward()
+            st, bits = db.status()
+        finally:
+            pa.testing_set_wait_limit(0)
+        if st == pa.PA_ERR_TIMEOUT:
+            break
+        pa.pa_status_clear(db.workspace)
     assert st == pa.PA_ERR_TIMEOUT, (pa.status_string(st), bits)
     assert bits & pa.PA_STATUS_BIT_TIMEOUT
     # the context is still usable: the same batch, with the default limit and a
