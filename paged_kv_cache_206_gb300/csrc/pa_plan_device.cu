@@ -5,10 +5,12 @@
 // plan, attention, combine -- is a fixed sequence of launches whose sizes do
 // not depend on the lengths, so it can be recorded once and replayed.
 //
-// One CTA of 1024 threads: sequence b is owned by threads b and b + 1024 of
-// the first pass; per-sequence counts are prefix-summed by warp 0 (64
-// sequences per lane, then a warp scan); every thread then writes items and
-// combine entries, finding its sequence by binary search over the offsets.
+// One CTA of 1024 threads; thread t owns sequences 2t and 2t + 1 through the
+// counting passes (their lengths stay in registers), the per-sequence counts
+// are turned into offsets by one block-wide scan, and every thread then writes
+// items and combine entries, finding its sequence by binary search over the
+// offsets. Per-sequence arithmetic is 32-bit (lengths are int32 and checked);
+// totals are 64-bit and checked against int32.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -22,18 +24,29 @@ namespace pa {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kPerLane = (PA_MAX_BATCH + 31) / 32;  // sequences per lane of the scan
+constexpr int kPerThread = 2;  // sequences a thread owns
+static_assert(kPlanThreads * kPerThread >= PA_MAX_BATCH, "every sequence has an owner");
 
-__device__ __forceinline__ int64_t dcdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__device__ __forceinline__ int cdiv32(int a, int b) { return a / b + (a % b != 0); }
 
+// Query rows G * q of a sequence. A launch whose total query tokens times
+// heads passes INT32_MAX is rejected (as pa_plan rejects it), and G * q is at
+// most that; the clamp only keeps the arithmetic of such a launch defined
+// until the rejection.
+__device__ __forceinline__ int rows_of(int G, int q) {
+  const int64_t r = int64_t(G) * q;
+  return int(r < INT32_MAX ? r : INT32_MAX);
+}
+
+// Sum of v over the CTA (all threads call it; the result is the CTA's).
 __device__ int64_t block_sum64(int64_t v, int64_t* red) {
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __syncthreads();
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  int64_t t = 0;
-  for (int w = 0; w < kPlanThreads / 32; ++w) t += red[w];
+  int64_t t = lane < kPlanThreads / 32 ? red[lane] : 0;
+  for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
   return t;
 }
 
@@ -49,14 +62,14 @@ __device__ __forceinline__ int find_owner(const int32_t* off, int n, int32_t x) 
 }
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanParams D) {
-  __shared__ int32_t off_it[PA_MAX_BATCH + 1];  // items before sequence b
-  __shared__ int32_t off_cb[PA_MAX_BATCH + 1];  // combine entries before b
-  __shared__ int32_t off_pr[PA_MAX_BATCH + 1];  // partial rows before b
-  __shared__ int32_t off_q[PA_MAX_BATCH + 1];   // query tokens before b
+  constexpr int kV = 4;  // counts per sequence: items, combine entries, partial rows, query tokens
+  __shared__ int32_t off[kV][PA_MAX_BATCH + 1];  // exclusive offsets, off[.][B] the totals
   __shared__ int64_t red[kPlanThreads / 32];
+  __shared__ int64_t wsum[kPlanThreads / 32][kV];  // warp totals, then their exclusive offsets
+  __shared__ int64_t tot[kV];
   __shared__ int err, chunk_s, max_nb_s;
   __shared__ int64_t cost_s[kPlanThreads / 32];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = D.batch, Hk = D.kv_heads, G = D.group, bs = D.block_size, TR = D.tr;
   if (tid == 0) {
     err = 0;
@@ -64,51 +77,65 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanPara
   }
   __syncthreads();
 
-  // pass 0: checks and the work measure of the automatic chunk rule
+  // pass 0: this thread's sequences, their checks and the work measure of the
+  // automatic chunk rule
+  int Ls[kPerThread], qs[kPerThread];
   int64_t w = 0;
   int mnb = 0;
-  for (int b = tid; b < B; b += kPlanThreads) {
-    const int64_t L = D.context_lens[b];
-    const int64_t q = D.q_seqlens ? D.q_seqlens[b] : 1;
-    const int64_t NB = dcdiv(L, bs);
-    if (q < 1 || q > D.maxq || L < q || NB > D.max_blocks_per_seq) {
+#pragma unroll
+  for (int k = 0; k < kPerThread; ++k) {
+    const int b = kPerThread * tid + k;
+    Ls[k] = 1;
+    qs[k] = 1;
+    if (b >= B) continue;
+    const int L = D.context_lens[b];
+    const int q = D.q_seqlens ? D.q_seqlens[b] : 1;
+    Ls[k] = L;
+    qs[k] = q;
+    if (q < 1 || q > D.maxq || L < q) {
       atomicOr(&err, 1);
       continue;
     }
-    w += NB * Hk * dcdiv(G * q, TR);
-    mnb = NB > mnb ? int(NB) : mnb;
+    const int NB = cdiv32(L, bs);
+    if (NB > D.max_blocks_per_seq) {
+      atomicOr(&err, 1);
+      continue;
+    }
+    w += int64_t(NB) * Hk * cdiv32(rows_of(G, q), TR);
+    mnb = NB > mnb ? NB : mnb;
   }
-  atomicMax(&max_nb_s, mnb);
+  if (mnb) atomicMax(&max_nb_s, mnb);
   const int64_t W = block_sum64(w, red);
   if (tid == 0) {
     int64_t c = D.chunk_blocks;
     if (c <= 0) {
-      c = dcdiv(W, (TR <= PA_FMA_MAX_ROWS ? 8 : 2) * int64_t(D.num_sms));
+      c = (W + (TR <= PA_FMA_MAX_ROWS ? 8 : 2) * int64_t(D.num_sms) - 1) /
+          ((TR <= PA_FMA_MAX_ROWS ? 8 : 2) * int64_t(D.num_sms));
       const int64_t RT = TR < int64_t(G) * D.maxq ? TR : int64_t(G) * D.maxq;  // real rows
-      const int64_t lo = dcdiv(int64_t(64) * RT * D.hv, int64_t(bs) * (D.hk + D.hv));
+      const int64_t den = int64_t(bs) * (D.hk + D.hv);
+      const int64_t lo = (int64_t(64) * RT * D.hv + den - 1) / den;
       if (lo > c) c = lo;
       if (c < 1) c = 1;
     }
     chunk_s = int(c < INT32_MAX ? c : INT32_MAX);
   }
   __syncthreads();
-  if (D.chunk_blocks <= 0 && TR > PA_FMA_MAX_ROWS) {
+  if (D.chunk_blocks <= 0 && TR > PA_FMA_MAX_ROWS && err == 0) {
     // wave fit (one CTA per SM): warp j prices the chunk c0 + j as its
     // waves x chunk; thread 0 takes the least, the first on a tie
-    const int warp = tid >> 5, lane = tid & 31;
-    const int64_t c0 = chunk_s, cc = c0 + warp;
-    const bool cand = cc <= wave_fit_hi(c0, max_nb_s);
+    const int64_t c0 = chunk_s, cc64 = c0 + warp;
+    const bool cand = cc64 <= wave_fit_hi(c0, max_nb_s);
+    const int cc = int(cand ? cc64 : 1);
     int64_t n = 0;
     if (cand) {
       for (int b = lane; b < B; b += 32) {
-        const int64_t L = D.context_lens[b];
-        const int64_t q = D.q_seqlens ? D.q_seqlens[b] : 1;
-        if (q < 1 || L < q) continue;  // reported through err
-        n += int64_t(Hk) * dcdiv(int64_t(G) * q, TR) * dcdiv(dcdiv(L, bs), cc);
+        const int L = D.context_lens[b];
+        const int q = D.q_seqlens ? D.q_seqlens[b] : 1;
+        n += int64_t(Hk) * cdiv32(rows_of(G, q), TR) * cdiv32(cdiv32(L, bs), cc);
       }
     }
     for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-    if (lane == 0) cost_s[warp] = cand ? dcdiv(n, int64_t(D.num_sms)) * cc : -1;
+    if (lane == 0) cost_s[warp] = cand ? (n + D.num_sms - 1) / D.num_sms * cc64 : -1;
     __syncthreads();
     if (tid == 0) {
       int64_t best = c0, best_cost = -1;
@@ -123,89 +150,83 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanPara
     }
     __syncthreads();
   }
-  const int64_t c = chunk_s;
+  const int c = chunk_s;
 
-  // pass 1: per-sequence counts (64-bit totals checked against int32)
-  int64_t t_it = 0, t_pr = 0, t_q = 0;
-  for (int b = tid; b < B; b += kPlanThreads) {
-    const int64_t L = D.context_lens[b];
-    const int64_t q = D.q_seqlens ? D.q_seqlens[b] : 1;
-    const int64_t NB = dcdiv(L > 0 ? L : 1, bs);
-    const int64_t R = G * q, QT = dcdiv(R, TR), S = dcdiv(NB, c);
-    const int64_t items = Hk * QT * S;
-    const int64_t prows = S > 1 ? Hk * S * R : 0;
-    t_it += items;
-    t_pr += prows;
-    t_q += q;
-    off_it[b] = int32_t(items < INT32_MAX ? items : INT32_MAX);
-    off_cb[b] = int32_t(S > 1 ? Hk * QT : 0);
-    off_pr[b] = int32_t(prows < INT32_MAX ? prows : INT32_MAX);
-    off_q[b] = int32_t(q);
+  // pass 1: per-sequence counts, then their exclusive offsets by one scan
+  // over the CTA (warp scans, a scan of the warp totals, the two added)
+  int64_t v[kPerThread][kV], incl[kV];
+#pragma unroll
+  for (int j = 0; j < kV; ++j) incl[j] = 0;
+#pragma unroll
+  for (int k = 0; k < kPerThread; ++k) {
+    const int b = kPerThread * tid + k;
+    const int L = Ls[k] > 0 ? Ls[k] : 1, q = qs[k] > 0 ? qs[k] : 1;
+    const int NB = cdiv32(L, bs), R = rows_of(G, q), QT = cdiv32(R, TR), S = cdiv32(NB, c);
+    const bool on = b < B && err == 0;
+    v[k][0] = on ? int64_t(Hk) * QT * S : 0;
+    v[k][1] = on && S > 1 ? int64_t(Hk) * QT : 0;
+    v[k][2] = on && S > 1 ? int64_t(Hk) * S * R : 0;
+    v[k][3] = on ? q : 0;
+#pragma unroll
+    for (int j = 0; j < kV; ++j) incl[j] += v[k][j];
   }
-  const int64_t n_items = block_sum64(t_it, red);
-  const int64_t n_prows = block_sum64(t_pr, red);
-  const int64_t n_q = block_sum64(t_q, red);
-  if (tid == 0) {
-    if (n_items > INT32_MAX || n_prows > INT32_MAX || n_q * D.num_heads > INT32_MAX)
-      err |= 1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+      const int64_t t = __shfl_up_sync(0xffffffffu, incl[j], o);
+      if (lane >= o) incl[j] += t;
+    }
+  }
+  if (lane == 31) {
+#pragma unroll
+    for (int j = 0; j < kV; ++j) wsum[warp][j] = incl[j];
   }
   __syncthreads();
-
-  // exclusive prefix sums over the sequences (warp 0)
-  if (tid < 32) {
-    const int lane = tid;
-    const int b0 = lane * kPerLane;
-    int32_t s_it = 0, s_cb = 0, s_pr = 0, s_q = 0;
-    for (int k = 0; k < kPerLane; ++k) {
-      const int b = b0 + k;
-      if (b < B) {
-        s_it += off_it[b];
-        s_cb += off_cb[b];
-        s_pr += off_pr[b];
-        s_q += off_q[b];
-      }
-    }
-    int32_t e_it = s_it, e_cb = s_cb, e_pr = s_pr, e_q = s_q;  // inclusive, then exclusive
+  if (warp == 0) {
+    int64_t x[kV], e[kV];
+#pragma unroll
+    for (int j = 0; j < kV; ++j) x[j] = e[j] = wsum[lane][j];
+#pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int32_t a = __shfl_up_sync(0xffffffffu, e_it, o);
-      const int32_t bb = __shfl_up_sync(0xffffffffu, e_cb, o);
-      const int32_t cc = __shfl_up_sync(0xffffffffu, e_pr, o);
-      const int32_t dd = __shfl_up_sync(0xffffffffu, e_q, o);
-      if (lane >= o) {
-        e_it += a;
-        e_cb += bb;
-        e_pr += cc;
-        e_q += dd;
+#pragma unroll
+      for (int j = 0; j < kV; ++j) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, e[j], o);
+        if (lane >= o) e[j] += t;
       }
     }
-    e_it -= s_it;
-    e_cb -= s_cb;
-    e_pr -= s_pr;
-    e_q -= s_q;
-    for (int k = 0; k < kPerLane; ++k) {
-      const int b = b0 + k;
-      if (b < B) {
-        const int32_t vi = off_it[b], vc = off_cb[b], vp = off_pr[b], vq = off_q[b];
-        off_it[b] = e_it;
-        off_cb[b] = e_cb;
-        off_pr[b] = e_pr;
-        off_q[b] = e_q;
-        e_it += vi;
-        e_cb += vc;
-        e_pr += vp;
-        e_q += vq;
-      }
-    }
-    if (lane == 31) {
-      off_it[B] = e_it;
-      off_cb[B] = e_cb;
-      off_pr[B] = e_pr;
-      off_q[B] = e_q;
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+      wsum[lane][j] = e[j] - x[j];  // exclusive offset of warp `lane`
+      if (lane == 31) tot[j] = e[j];
     }
   }
   __syncthreads();
+  if (tid == 0) {
+    if (tot[0] > INT32_MAX || tot[2] > INT32_MAX || tot[3] * D.num_heads > INT32_MAX) err |= 1;
+  }
+#pragma unroll
+  for (int j = 0; j < kV; ++j) {
+    // exclusive offset of this thread's first sequence
+    int64_t base = wsum[warp][j] + incl[j] - (v[0][j] + v[1][j]);
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      const int b = kPerThread * tid + k;
+      if (b < B) off[j][b] = int32_t(base < INT32_MAX ? base : INT32_MAX);
+      base += v[k][j];
+    }
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int j = 0; j < kV; ++j) off[j][B] = int32_t(tot[j] < INT32_MAX ? tot[j] : INT32_MAX);
+  }
+  __syncthreads();
+  const int32_t* off_it = off[0];
+  const int32_t* off_cb = off[1];
+  const int32_t* off_pr = off[2];
+  const int32_t* off_q = off[3];
   const int32_t N_it = off_it[B], N_cb = off_cb[B];
-  bool fail = err != 0;
+  const bool fail = err != 0;
   const bool small = !fail && (N_it > D.work_cap || N_cb > D.comb_cap);
   if (fail || small) {
     if (tid == 0) {
@@ -221,37 +242,37 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanPara
   // the lists, in (b, kvh, qt, split) order
   for (int x = tid; x < N_it; x += kPlanThreads) {
     const int b = find_owner(off_it, B, x);
-    const int64_t L = D.context_lens[b];
-    const int64_t q = D.q_seqlens ? D.q_seqlens[b] : 1;
-    const int64_t NB = dcdiv(L, bs), R = G * q, QT = dcdiv(R, TR), S = dcdiv(NB, c);
-    const int64_t local = x - off_it[b];
-    const int64_t kvh = local / (QT * S), rem = local % (QT * S);
-    const int64_t qt = rem / S, s = rem % S;
-    const int64_t r0 = qt * TR, r1 = R < r0 + TR ? R : r0 + TR;
+    const int L = D.context_lens[b];
+    const int q = D.q_seqlens ? D.q_seqlens[b] : 1;
+    const int NB = cdiv32(L, bs), R = rows_of(G, q), QT = cdiv32(R, TR), S = cdiv32(NB, c);
+    const int local = x - off_it[b];
+    const int kvh = local / (QT * S), rem = local % (QT * S);
+    const int qt = rem / S, s = rem % S;
+    const int r0 = qt * TR, r1 = R < r0 + TR ? R : r0 + TR;
     int32_t* e = D.work + int64_t(x) * PA_WORK_INTS;
     e[0] = b;
-    e[1] = int32_t(kvh);
-    e[2] = int32_t(r0);
-    e[3] = int32_t(r1);
-    e[4] = int32_t(s * c);
-    e[5] = int32_t(NB < (s + 1) * c ? NB : (s + 1) * c);
+    e[1] = kvh;
+    e[2] = r0;
+    e[3] = r1;
+    e[4] = s * c;
+    e[5] = NB < (s + 1) * c ? NB : (s + 1) * c;
     e[6] = off_q[b];
     // partial rows of sequence b run (kvh, qt, s) in order: S * R per kv
     // head, S * TR per full row tile before qt, then this tile's rows per split
-    e[7] = S > 1 ? int32_t(off_pr[b] + kvh * S * R + qt * TR * S + s * (r1 - r0)) : -1;
+    e[7] = S > 1 ? off_pr[b] + kvh * S * R + qt * TR * S + s * (r1 - r0) : -1;
   }
   for (int y = tid; y < N_cb; y += kPlanThreads) {
     const int b = find_owner(off_cb, B, y);
-    const int64_t L = D.context_lens[b];
-    const int64_t q = D.q_seqlens ? D.q_seqlens[b] : 1;
-    const int64_t NB = dcdiv(L, bs), QT = dcdiv(G * q, TR), S = dcdiv(NB, c);
-    const int64_t local = y - off_cb[b];
-    const int64_t kvh = local / QT, qt = local % QT;
+    const int L = D.context_lens[b];
+    const int q = D.q_seqlens ? D.q_seqlens[b] : 1;
+    const int NB = cdiv32(L, bs), QT = cdiv32(rows_of(G, q), TR), S = cdiv32(NB, c);
+    const int local = y - off_cb[b];
+    const int kvh = local / QT, qt = local % QT;
     int32_t* e = D.combine + int64_t(y) * PA_COMBINE_INTS;
     e[0] = b;
-    e[1] = int32_t(kvh);
-    e[2] = int32_t(off_it[b] + (kvh * QT + qt) * S);
-    e[3] = int32_t(S);
+    e[1] = kvh;
+    e[2] = off_it[b] + (kvh * QT + qt) * S;
+    e[3] = S;
   }
   if (tid == 0) {
     D.counts[0] = N_it;

@@ -80,7 +80,7 @@ def random_case(seed):
     return cfg, ctx, ql
 
 
-@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("seed", range(24))
 def test_device_plan_equals_host_plan(seed):
     cfg, ctx, ql = random_case(seed)
     host = pa.pa_plan(cfg, ctx, ql)
