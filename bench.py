@@ -521,12 +521,14 @@ def measure(name, args, steps, dev, stream, flush, rank, peaks_, read_gbs, cpu_s
             "h2d_bytes_per_step": int(gs.h2d_bytes),
             "d2h_bytes_per_step": int(gs.out.numel() * gs.out.element_size()),
             "ms_per_step": e2e_all * 1e3,
-            "path": "GraphStep: one graph replay per step (copy in, device plan, attention, "
-                    "copy out), host waits",
+            "path": "GraphStep: one graph replay per step (device plan reading the lengths "
+                    "from pinned host memory, beside the copy of the inputs; attention, "
+                    "combine, copy out), host waits",
             "breakdown_us": {"h2d_copy": stages[0], "plan_device": stages[1],
                              "attention": stages[2], "d2h_copy": stages[3],
-                             "how": "the graph's stages enqueued directly on its stream behind "
-                                    "the L2 flush, CUDA events between them"},
+                             "how": "the graph's stages enqueued one after another (the whole "
+                                    "arena copied first, no overlap) on its stream behind the L2 "
+                                    "flush, CUDA events between them"},
             "host_planned": {"value": kv_all / host_all / 1e9, "ms_per_step": host_all * 1e3,
                              "h2d_bytes_per_step": int(hs.last_h2d_bytes),
                              "path": "HostStep: pa_plan on the host, direct launches"}},

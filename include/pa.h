@@ -316,8 +316,11 @@ pa_status pa_plan_bounds(const pa_config* cfg, int64_t* work_cap, int64_t* comb_
 /*
  * pa_plan_device -- pa_plan on the GPU (asynchronous, one small kernel).
  *
- * context_lens, q_seqlens  device int32 [batch] (q_seqlens may be NULL)
- * work, combine  device int32 [work_cap * PA_WORK_INTS], [comb_cap * PA_COMBINE_INTS]
+ * context_lens, q_seqlens  int32 [batch] the device can read: device memory, or
+ *                pinned host memory mapped into its address space;
+ *                q_seqlens may be NULL
+ * work, combine  device int32 [work_cap * PA_WORK_INTS], [comb_cap * PA_COMBINE_INTS],
+ *                16-byte aligned
  * counts         device int32 [PA_PLAN_COUNTS]: items, combine entries,
  *                partial rows, error (0 ok, 1 a length breaks a constraint, 2
  *                a capacity is too small)

@@ -479,14 +479,16 @@ class DevicePlanStep:
 class GraphStep:
     """One attention step recorded once as a CUDA graph and replayed per step.
 
-    The step's inputs live in one pinned host arena (views ``query``,
-    ``block_tables``, ``context_lens``, ``q_seqlens``). The graph holds: one
-    host-to-device copy of the arena, the device planner (pa_plan_device), the
-    forward pass over its lists (pa_forward_device_plan) and the copy of the
-    output back into the pinned ``out`` tensor. :meth:`run` replays it and
-    waits, so a decode loop costs one graph launch per step. The launches do
-    not depend on the lengths (grids are pa_plan_bounds' capacities), which is
-    what allows the recording.
+    The step's inputs live in one pinned host arena (views ``context_lens``,
+    ``q_seqlens``, ``query``, ``block_tables``). The graph holds: the device
+    planner (pa_plan_device), reading the lengths straight from the pinned
+    arena (mapped into the device's address space), beside it on a second
+    stream the host-to-device copy of the arena, then the forward pass over
+    the planner's lists (pa_forward_device_plan) and the copy of the output
+    back into the pinned ``out`` tensor. :meth:`run` replays it and waits, so
+    a decode loop costs one graph launch per step.
+    The launches do not depend on the lengths (grids are pa_plan_bounds'
+    capacities), which is what allows the recording.
     """
 
     def __init__(self, cfg: pa_config, key_cache, value_cache, total_q: int, mask=None,
@@ -499,9 +501,9 @@ class GraphStep:
         B, H, hk, hv = cfg.batch, cfg.num_heads, cfg.head_size_k, cfg.head_size_v
         has_ql = cfg.max_seqlen_q > 1
         self.total_q = int(total_q)
-        sizes = [("query", self.total_q * H * hk * 2),
-                 ("block_tables", B * cfg.max_blocks_per_seq * 4),
-                 ("context_lens", B * 4), ("q_seqlens", B * 4 if has_ql else 0)]
+        sizes = [("context_lens", B * 4), ("q_seqlens", B * 4 if has_ql else 0),
+                 ("query", self.total_q * H * hk * 2),
+                 ("block_tables", B * cfg.max_blocks_per_seq * 4)]
         self.offsets, off = {}, 0
         for name, n in sizes:
             self.offsets[name] = off
@@ -533,26 +535,45 @@ class GraphStep:
         self.out = torch.empty((self.total_q, H, hv), dtype=torch.float16).pin_memory()
         self.h2d_bytes = self.arena_bytes
         self.stream = torch.cuda.Stream(device=dev)
+        self.side_stream = torch.cuda.Stream(device=dev)
         self.graph = None
 
     def _enqueue(self, events=None):
-        """Enqueue the step's stages on its stream; with ``events`` (five CUDA
-        events), record one before the host-to-device copy and one after each
-        stage (copy in, device planner, attention, copy out)."""
+        """Enqueue the step on its stream. Without ``events`` (the recorded
+        graph), the copy of the query and block tables runs on a second stream
+        beside the device planner, which needs only the lengths. With
+        ``events`` (five CUDA events) the stages run one after another, an event
+        recorded before the host-to-device copy and after each stage (copy in,
+        device planner, attention, copy out), to time them separately."""
         import torch
         lib, cfg, s = load_library(), self.cfg, self.stream
 
         def mark(k):
             if events is not None:
                 events[k].record(s)
+
+        def plan(cl, ql):
+            _check(lib.pa_plan_device(
+                ctypes.byref(cfg), _tptr(cl), _tptr(ql), _tptr(self.work),
+                self.work_cap, _tptr(self.combine), self.comb_cap, _tptr(self.counts),
+                _tptr(self.workspace), ctypes.c_void_p(s.cuda_stream)), "pa_plan_device")
+
         mark(0)
-        with torch.cuda.stream(s):
-            self.d_arena.copy_(self.h_arena, non_blocking=True)
-        mark(1)
-        _check(lib.pa_plan_device(
-            ctypes.byref(cfg), _tptr(self._dcl), _tptr(self._dql), _tptr(self.work),
-            self.work_cap, _tptr(self.combine), self.comb_cap, _tptr(self.counts),
-            _tptr(self.workspace), ctypes.c_void_p(s.cuda_stream)), "pa_plan_device")
+        if events is None:
+            # the planner reads the lengths from the pinned arena itself (a
+            # few KB over the host link) while the arena's copy, which the
+            # forward pass needs, runs beside it
+            side = self.side_stream
+            side.wait_stream(s)
+            plan(self.context_lens, self.q_seqlens)
+            with torch.cuda.stream(side):
+                self.d_arena.copy_(self.h_arena, non_blocking=True)
+            s.wait_stream(side)
+        else:
+            with torch.cuda.stream(s):
+                self.d_arena.copy_(self.h_arena, non_blocking=True)
+            mark(1)
+            plan(self._dcl, self._dql)
         mark(2)
         _check(lib.pa_forward_device_plan(
             ctypes.byref(cfg), _tptr(self._dq), _tptr(self.key_cache), _tptr(self.value_cache),

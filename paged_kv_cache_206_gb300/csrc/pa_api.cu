@@ -391,7 +391,9 @@ extern "C" pa_status pa_plan_device(const pa_config* cfg, const int32_t* context
   if (c.chunk_blocks < 0 || (c.chunk_blocks == 0 && c.num_sms <= 0)) return PA_ERR_INVALID_ARG;
   if (work_cap < 1 || comb_cap < 0 || work_cap > INT32_MAX || comb_cap > INT32_MAX)
     return PA_ERR_INVALID_ARG;
-  if (!aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+  // the planner writes an item as two 16-byte stores, a combine entry as one
+  if (!aligned(workspace, 256) || !aligned(work, 16) || (combine && !aligned(combine, 16)))
+    return PA_ERR_INVALID_ARG;
   DevPlanParams D{};
   D.context_lens = context_lens;
   D.q_seqlens = q_seqlens;

@@ -64,6 +64,7 @@ __device__ __forceinline__ int find_owner(const int32_t* off, int n, int32_t x) 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanParams D) {
   constexpr int kV = 4;  // counts per sequence: items, combine entries, partial rows, query tokens
   __shared__ int32_t off[kV][PA_MAX_BATCH + 1];  // exclusive offsets, off[.][B] the totals
+  __shared__ int32_t nb_s[PA_MAX_BATCH];         // KV blocks of each sequence
   __shared__ int64_t red[kPlanThreads / 32];
   __shared__ int64_t wsum[kPlanThreads / 32][kV];  // warp totals, then their exclusive offsets
   __shared__ int64_t tot[kV];
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanPara
     const int L = Ls[k] > 0 ? Ls[k] : 1, q = qs[k] > 0 ? qs[k] : 1;
     const int NB = cdiv32(L, bs), R = rows_of(G, q), QT = cdiv32(R, TR), S = cdiv32(NB, c);
     const bool on = b < B && err == 0;
+    if (b < B) nb_s[b] = NB;
     v[k][0] = on ? int64_t(Hk) * QT * S : 0;
     v[k][1] = on && S > 1 ? int64_t(Hk) * QT : 0;
     v[k][2] = on && S > 1 ? int64_t(Hk) * S * R : 0;
@@ -239,40 +241,32 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const DevPlanPara
     return;
   }
 
-  // the lists, in (b, kvh, qt, split) order
+  // the lists, in (b, kvh, qt, split) order, from shared memory alone (a
+  // sequence's query tokens are the difference of its offsets); an item is
+  // two 16-byte stores, a combine entry one
   for (int x = tid; x < N_it; x += kPlanThreads) {
     const int b = find_owner(off_it, B, x);
-    const int L = D.context_lens[b];
-    const int q = D.q_seqlens ? D.q_seqlens[b] : 1;
-    const int NB = cdiv32(L, bs), R = rows_of(G, q), QT = cdiv32(R, TR), S = cdiv32(NB, c);
+    const int q = off_q[b + 1] - off_q[b];
+    const int NB = nb_s[b], R = rows_of(G, q), QT = cdiv32(R, TR), S = cdiv32(NB, c);
     const int local = x - off_it[b];
     const int kvh = local / (QT * S), rem = local % (QT * S);
     const int qt = rem / S, s = rem % S;
     const int r0 = qt * TR, r1 = R < r0 + TR ? R : r0 + TR;
-    int32_t* e = D.work + int64_t(x) * PA_WORK_INTS;
-    e[0] = b;
-    e[1] = kvh;
-    e[2] = r0;
-    e[3] = r1;
-    e[4] = s * c;
-    e[5] = NB < (s + 1) * c ? NB : (s + 1) * c;
-    e[6] = off_q[b];
     // partial rows of sequence b run (kvh, qt, s) in order: S * R per kv
     // head, S * TR per full row tile before qt, then this tile's rows per split
-    e[7] = S > 1 ? off_pr[b] + kvh * S * R + qt * TR * S + s * (r1 - r0) : -1;
+    const int slot = S > 1 ? off_pr[b] + kvh * S * R + qt * TR * S + s * (r1 - r0) : -1;
+    int4* e = reinterpret_cast<int4*>(D.work + int64_t(x) * PA_WORK_INTS);
+    e[0] = make_int4(b, kvh, r0, r1);
+    e[1] = make_int4(s * c, NB < (s + 1) * c ? NB : (s + 1) * c, off_q[b], slot);
   }
   for (int y = tid; y < N_cb; y += kPlanThreads) {
     const int b = find_owner(off_cb, B, y);
-    const int L = D.context_lens[b];
-    const int q = D.q_seqlens ? D.q_seqlens[b] : 1;
-    const int NB = cdiv32(L, bs), QT = cdiv32(rows_of(G, q), TR), S = cdiv32(NB, c);
+    const int q = off_q[b + 1] - off_q[b];
+    const int NB = nb_s[b], QT = cdiv32(rows_of(G, q), TR), S = cdiv32(NB, c);
     const int local = y - off_cb[b];
     const int kvh = local / QT, qt = local % QT;
-    int32_t* e = D.combine + int64_t(y) * PA_COMBINE_INTS;
-    e[0] = b;
-    e[1] = kvh;
-    e[2] = off_it[b] + (kvh * QT + qt) * S;
-    e[3] = S;
+    *reinterpret_cast<int4*>(D.combine + int64_t(y) * PA_COMBINE_INTS) =
+        make_int4(b, kvh, off_it[b] + (kvh * QT + qt) * S, S);
   }
   if (tid == 0) {
     D.counts[0] = N_it;

@@ -126,6 +126,8 @@ def test_plan_bounds_and_device_plan_host_checks(lib):
     assert dev(c, wcap=0) == pa.PA_ERR_INVALID_ARG
     assert dev(c, comb=None) == pa.PA_ERR_INVALID_ARG
     assert dev(c, ws=ctypes.c_void_p((1 << 20) + 64)) == pa.PA_ERR_INVALID_ARG
+    assert dev(c, work=ctypes.c_void_p((1 << 20) + 4)) == pa.PA_ERR_INVALID_ARG  # 16-byte stores
+    assert dev(c, comb=ctypes.c_void_p((1 << 20) + 8)) == pa.PA_ERR_INVALID_ARG
     assert dev(_cfg(block_size=8)) == pa.PA_ERR_INVALID_ARG
     assert dev(_cfg(mask_type=4)) == pa.PA_ERR_UNSUPPORTED
     # the automatic chunk rule needs the SM count (the device planner divides by it)
