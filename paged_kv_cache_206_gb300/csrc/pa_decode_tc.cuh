@@ -453,52 +453,126 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     __syncwarp();
   } else if (warp == 1) {
     // ================= QK issuer =================
-    // S^T(m) into buffer m & 1 once the softmax has read S^T(m - 2).
-    bool ok = true;
-    const uint32_t q_addr = smem_u32(q_s), ring_addr = smem_u32(kring);
-    int consumed = 0;
-    // the softmax warps load the query tile while the producers already stream
-    if (ntiles > 0 && !warp_wait(q_ready, 0, lane, P.wait_limit)) ok = false;
-    for (int m = 0; m < ntiles && ok; ++m) {
-      if (m >= 2 && !warp_wait(&s_free[m & 1], ((m >> 1) - 1) & 1, lane, P.wait_limit)) { ok = false; break; }
-      tc_fence_after();
-      for (int ks = 0; ks < KS; ++ks, ++consumed) {
-        const int slot = consumed % kKSlots;
-        if (!warp_wait(&kfull[slot], (consumed / kKSlots) & 1, lane, P.wait_limit)) { ok = false; break; }
-        tc_fence_after();
-        if (lane == 0) {
+    if constexpr (SH) {
+      // S^T(m) into buffer m & 1 once the softmax has read S^T(m - 2). Lane 0
+      // alone waits and issues (a tcgen05.mma costs about 50 cycles to issue
+      // whatever its shape, and the issue of these small ones is what paces a
+      // narrow tile of the shared 576/512 cache): no warp-wide exchange per
+      // slot. Separate caches keep the warp-wide form below.
+      if (lane == 0) {
+        bool ok = true;
+        const uint32_t q_addr = smem_u32(q_s), ring_addr = smem_u32(kring);
+        int consumed = 0;
+        // the query tile (TMA or the softmax warps' loads) while the producers stream
+        if (ntiles > 0 && !mbar_wait(q_ready, 0, P.wait_limit)) ok = false;
+        for (int m = 0; m < ntiles && ok; ++m) {
+          if (m >= 2 && !mbar_wait(&s_free[m & 1], ((m >> 1) - 1) & 1, P.wait_limit)) { ok = false; break; }
+          tc_fence_after();
+          for (int ks = 0; ks < KS; ++ks, ++consumed) {
+            const int slot = consumed % kKSlots;
+            if (!mbar_wait(&kfull[slot], (consumed / kKSlots) & 1, P.wait_limit)) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (2 * ks + h >= KH) break;  // an odd KH leaves the last slot one half
+            for (int h = 0; h < 2; ++h) {
+              if (2 * ks + h >= KH) break;  // an odd KH leaves the last slot one half
+              const uint64_t a = smem_desc(ring_addr + slot * kTcSlotBytes + h * kTcHalfBytes, 16, 1024);
+              const uint64_t b = smem_desc(q_addr + (2 * ks + h) * (NR * 128), 16, 1024);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t a = smem_desc(ring_addr + slot * kTcSlotBytes + h * kTcHalfBytes + k * 32, 16, 1024);
-              const uint64_t b = smem_desc(q_addr + (2 * ks + h) * (NR * 128) + k * 32, 16, 1024);
-              tc_mma(tmem_s + (m & 1) * 64, a, b, kIdescQK, (ks | h | k) != 0);
+              for (int k = 0; k < 4; ++k)  // +32 bytes a k-step: +2 in the address field
+                tc_mma(tmem_s + (m & 1) * 64, a + 2 * k, b + 2 * k, kIdescQK, (ks | h | k) != 0);
             }
+            // (the slot is released after the PV: V is its first dims)
           }
-          if (!SH) tc_commit(&kempty[slot]);  // shared KV: released after the PV
+          if (!ok) break;
+          tc_commit(&s_full[m & 1]);
         }
+        if (!ok) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
+        tc_commit(qk_done);
+      }
+      __syncwarp();
+    } else {
+      // S^T(m) into buffer m & 1 once the softmax has read S^T(m - 2).
+      bool ok = true;
+      const uint32_t q_addr = smem_u32(q_s), ring_addr = smem_u32(kring);
+      int consumed = 0;
+      // the softmax warps load the query tile while the producers already stream
+      if (ntiles > 0 && !warp_wait(q_ready, 0, lane, P.wait_limit)) ok = false;
+      for (int m = 0; m < ntiles && ok; ++m) {
+        if (m >= 2 && !warp_wait(&s_free[m & 1], ((m >> 1) - 1) & 1, lane, P.wait_limit)) { ok = false; break; }
+        tc_fence_after();
+        for (int ks = 0; ks < KS; ++ks, ++consumed) {
+          const int slot = consumed % kKSlots;
+          if (!warp_wait(&kfull[slot], (consumed / kKSlots) & 1, lane, P.wait_limit)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (2 * ks + h >= KH) break;  // an odd KH leaves the last slot one half
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t a = smem_desc(ring_addr + slot * kTcSlotBytes + h * kTcHalfBytes + k * 32, 16, 1024);
+                const uint64_t b = smem_desc(q_addr + (2 * ks + h) * (NR * 128) + k * 32, 16, 1024);
+                tc_mma(tmem_s + (m & 1) * 64, a, b, kIdescQK, (ks | h | k) != 0);
+              }
+            }
+            tc_commit(&kempty[slot]);
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit(&s_full[m & 1]);
         __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(&s_full[m & 1]);
+      if (!ok && lane == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
+      if (lane == 0) tc_commit(qk_done);
       __syncwarp();
     }
-    if (!ok && lane == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
-    if (lane == 0) tc_commit(qk_done);
-    __syncwarp();
   } else if (warp == 11) {
     // ================= PV issuer =================
+    // Shared-KV cache: lane 0 waits and issues a full tile alone, the whole
+    // warp joining only on a tile with rows past the range, to zero them.
+    // Separate caches keep the warp-wide waits (measured faster there: the
+    // lane-0 form changed the register allocation of the 64-row kernel).
     bool ok = true;
     uint8_t* const ring = SH ? kring : vring;  // shared KV: V is in the K slots
     const uint32_t p_addr = smem_u32(p_s), ring_addr = smem_u32(ring);
     int consumed = 0;
     for (int n = 0; n < ntiles && ok; ++n) {
       const int pb = n % kTcPBufs;
+      const int nvalid = min(kTcTok, it.tok1 - (it.tok0 + n * kTcTok));
+      if (SH && nvalid == kTcTok) {
+        // a full tile. Shared KV: chunk oc is K slot oc of tile n, whose
+        // copy the QK issuer has waited for (the wait here returns at once and
+        // orders this thread's reads after the copy).
+        if (lane == 0) {
+          ok = mbar_wait(&p_full[pb], (n / kTcPBufs) & 1, P.wait_limit);
+          tc_fence_after();
+          for (int oc = 0; oc < VS && ok; ++oc, ++consumed) {
+            const int seq = SH ? n * KS + oc : consumed;
+            const int ring_slots = SH ? kKSlots : kVSlots;
+            const int slot = seq % ring_slots;
+            if (!mbar_wait(SH ? &kfull[slot] : &vfull[slot], (seq / ring_slots) & 1, P.wait_limit)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t a = smem_desc(ring_addr + slot * kTcSlotBytes, kTcHalfBytes, 1024);
+            const uint64_t b = smem_desc(p_addr + pb * (kTcTok * 128), kTcHalfBytes, 1024);
+#pragma unroll
+            for (int k = 0; k < kTcTok / 16; ++k)  // +2048 bytes a k-step: +128 in the address field
+              tc_mma(tmem_o + oc * 64, a + 128 * k, b + 128 * k, kIdescPV, (n | k) != 0);
+            if (!SH) tc_commit(&vempty[slot]);
+          }
+          if (ok && SH)  // every K slot of tile n (the last one too) is free once its PV is done
+            for (int sl = 0; sl < KS; ++sl) tc_commit(&kempty[(n * KS + sl) % kKSlots]);
+          if (ok) tc_commit(&pv_done[pb]);
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        consumed = __shfl_sync(0xffffffffu, consumed, 0);
+        continue;
+      }
       if (!warp_wait(&p_full[pb], (n / kTcPBufs) & 1, lane, P.wait_limit)) { ok = false; break; }
       tc_fence_after();
-      const int nvalid = min(kTcTok, it.tok1 - (it.tok0 + n * kTcTok));
       for (int oc = 0; oc < VS; ++oc, ++consumed) {
         // shared KV: chunk oc is K slot oc of tile n (already waited on by the
         // QK issuer; this wait returns at once and orders the reads after the copy)
