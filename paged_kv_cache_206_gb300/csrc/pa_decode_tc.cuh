@@ -39,8 +39,8 @@ namespace pa {
 
 constexpr int kTcRows = PA_TC_TILE_ROWS;  // rows of a tile at most; N of the PV MMA
 constexpr int kTcTok = 64;                // tokens per tile (M of QK^T)
-constexpr int kTcPBufs = 1;               // P^T buffers (softmax of tile n + kTcPBufs
-                                          // waits for the PV of tile n)
+constexpr int kTcPBufs = 1;               // P^T buffers of separate caches (softmax of tile
+                                          // n + kTcPBufs waits for the PV of tile n)
 constexpr uint32_t kTcMaxSmem = 232448;   // dynamic shared memory a CTA may use
 constexpr uint32_t kTcHalfBytes = kTcTok * 128;      // 64 tokens x 64 dims x 2 B
 constexpr uint32_t kTcSlotBytes = 2 * kTcHalfBytes;  // 64 tokens x 128 dims
@@ -58,7 +58,10 @@ constexpr float kTcRescaleThreshold = 8.f;  // log2 units
 template <int HK, int NR, bool SH = false>
 struct TcCfg {
   static constexpr uint32_t kQBytes = uint32_t(HK / 64) * NR * 128;
-  static constexpr uint32_t kOther = kTcPBufs * kTcTok * 128 + 4 * kTcRows * 4 +
+  // The shared 576/512 cache is paced by the MMA issue: a second P^T buffer
+  // (one K slot less) lets the softmax of tile n + 1 run under the PV of tile n.
+  static constexpr int kPBufs = SH ? 2 : kTcPBufs;
+  static constexpr uint32_t kOther = kPBufs * kTcTok * 128 + 4 * kTcRows * 4 +
                                      6 * kTcRows * 4 + 12 * 8 + 16 + 1024;
   static constexpr int kFit = int((kTcMaxSmem - kQBytes - kOther) / (kTcSlotBytes + 16));
   static constexpr int kSlots = kFit < 12 ? kFit : 12;
@@ -66,7 +69,7 @@ struct TcCfg {
   static constexpr int kVSlots = SH ? 0 : kSlots / 2;
   static constexpr uint32_t q_off = 0;
   static constexpr uint32_t p_off = q_off + kQBytes;
-  static constexpr uint32_t ring_off = p_off + kTcPBufs * kTcTok * 128;  // 1024-aligned
+  static constexpr uint32_t ring_off = p_off + kPBufs * kTcTok * 128;  // 1024-aligned
   static constexpr uint32_t red_off = ring_off + kSlots * kTcSlotBytes;  // [4][64] fp32
   static constexpr uint32_t rows_off = red_off + 4 * kTcRows * 4;        // per-row constants
   static constexpr uint32_t bars_off = rows_off + 6 * kTcRows * 4;       // mbarriers
@@ -267,6 +270,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
   constexpr uint32_t kTmemCols = 512;
   using Cfg = TcCfg<HK, NR, SH>;
   constexpr int kKSlots = Cfg::kKSlots, kVSlots = Cfg::kVSlots;
+  constexpr int PB = Cfg::kPBufs;
   constexpr int RH = NR / 2;  // rows per softmax thread (two warps per lane quarter)
   constexpr uint32_t kIdescQK = mma_idesc(64, NR, 0, 0);
   // PV reads the first NR columns of each 128-byte P^T row (the tile's rows)
@@ -538,14 +542,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     const uint32_t p_addr = smem_u32(p_s), ring_addr = smem_u32(ring);
     int consumed = 0;
     for (int n = 0; n < ntiles && ok; ++n) {
-      const int pb = n % kTcPBufs;
+      const int pb = n % PB;
       const int nvalid = min(kTcTok, it.tok1 - (it.tok0 + n * kTcTok));
       if (SH && nvalid == kTcTok) {
         // a full tile. Shared KV: chunk oc is K slot oc of tile n, whose
         // copy the QK issuer has waited for (the wait here returns at once and
         // orders this thread's reads after the copy).
         if (lane == 0) {
-          ok = mbar_wait(&p_full[pb], (n / kTcPBufs) & 1, P.wait_limit);
+          ok = mbar_wait(&p_full[pb], (n / PB) & 1, P.wait_limit);
           tc_fence_after();
           for (int oc = 0; oc < VS && ok; ++oc, ++consumed) {
             const int seq = SH ? n * KS + oc : consumed;
@@ -571,7 +575,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         consumed = __shfl_sync(0xffffffffu, consumed, 0);
         continue;
       }
-      if (!warp_wait(&p_full[pb], (n / kTcPBufs) & 1, lane, P.wait_limit)) { ok = false; break; }
+      if (!warp_wait(&p_full[pb], (n / PB) & 1, lane, P.wait_limit)) { ok = false; break; }
       tc_fence_after();
       for (int oc = 0; oc < VS; ++oc, ++consumed) {
         // shared KV: chunk oc is K slot oc of tile n (already waited on by the
@@ -656,7 +660,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         }
       }
       if (NR < kTcRows)  // P^T columns past NR are read by the PV MMA: keep them zero
-        for (int i = st; i < kTcPBufs * kTcTok * 8; i += 256)
+        for (int i = st; i < PB * kTcTok * 8; i += 256)
           reinterpret_cast<uint4*>(p_s)[i] = make_uint4(0, 0, 0, 0);
       fence_proxy_async();  // written by threads, read by the tensor cores
       __syncwarp();
@@ -771,15 +775,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       }
 #pragma unroll
       for (int r = 0; r < RH; ++r) l_t[r] += s[r];
-      // P^T buffer n % kTcPBufs was last read by PV(n - kTcPBufs); a rescale
+      // P^T buffer n % PB was last read by PV(n - PB); a rescale
       // of O^T also needs PV(n - 1). Each wait is on the barrier of that PV's
       // P^T buffer, whose next phase needs P^T(n) and so cannot have begun.
       {
         bool pv = true;
         if (grew && n >= 1)
-          pv = mbar_wait(&pv_done[(n - 1) % kTcPBufs], ((n - 1) / kTcPBufs) & 1, P.wait_limit);
-        if (n >= kTcPBufs)
-          pv = pv && mbar_wait(&pv_done[n % kTcPBufs], ((n - kTcPBufs) / kTcPBufs) & 1, P.wait_limit);
+          pv = mbar_wait(&pv_done[(n - 1) % PB], ((n - 1) / PB) & 1, P.wait_limit);
+        if (n >= PB)
+          pv = pv && mbar_wait(&pv_done[n % PB], ((n - PB) / PB) & 1, P.wait_limit);
         if (softmax_bar_or(!pv)) { ok = false; break; }
         tc_fence_after();
       }
@@ -794,7 +798,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
           pk.z = pack_half2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
           pk.w = pack_half2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
           const int chunk = rh * (RH / 8) + c8;
-          *reinterpret_cast<uint4*>(p_s + (n % kTcPBufs) * (kTcTok * 128) + tt * 128 + ((chunk ^ (tt & 7)) << 4)) = pk;
+          *reinterpret_cast<uint4*>(p_s + (n % PB) * (kTcTok * 128) + tt * 128 + ((chunk ^ (tt & 7)) << 4)) = pk;
         }
       }
       if (grew) {
@@ -815,7 +819,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       fence_proxy_async();  // P^T is read by the tensor cores
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[n % kTcPBufs]);
+      if (lane == 0) mbar_arrive(&p_full[n % PB]);
     }
     const int t = quarter * 32 + lane;  // TMEM lane of this thread = output dim in a chunk
     if (!ok && t == 0 && rh == 0) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
