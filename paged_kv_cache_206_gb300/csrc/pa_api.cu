@@ -296,9 +296,9 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
   } else if (TR == PA_PF_TILE_ROWS || TR == PA_PF_PAIR_ROWS) {
     // rows meet many keys (more than one 64-row tile per kv head: 128-row
     // tiles, or 256-row tiles of two query tiles for prefill): 128-token key
-    // tiles, boxes of min(block_size, 128) tokens, both 64-dim halves in one
-    // box at 128
-    const int rows = c.block_size < 128 ? c.block_size : 128;
+    // tiles, boxes of the largest power of two (at most 128) dividing the
+    // block size, both 64-dim halves in one box at 128
+    const int rows = box_tokens(c.block_size, 128);
     const int halves = rows == 128 ? hk / 64 : 1;
     CUtensorMap tmk, tmv;
     if (!cache_map_3d(&tmk, key_cache, c, hk, rows, halves) ||
@@ -307,9 +307,10 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
     err = TR == PA_PF_PAIR_ROWS ? launch_pf_pair(tmk, tmv, P, n_items, stream)
                                 : launch_pf(tmk, tmv, P, n_items, stream);
   } else {
-    // 64-row tiles on the tcgen05 kernel: boxes of min(block_size, 64) tokens
+    // 64-row tiles on the tcgen05 kernel: boxes of the largest power of two
+    // (at most 64) dividing the block size
     if (!tc_supported(hk, hv)) return PA_ERR_UNSUPPORTED;
-    const int rows = c.block_size < 64 ? c.block_size : 64;
+    const int rows = box_tokens(c.block_size, 64);
     const int halves = rows == 64 ? 2 : 1;
     CUtensorMap tmk, tmv, tmq;
     if (!cache_map_3d(&tmk, key_cache, c, hk, rows, halves) ||

@@ -389,7 +389,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
           tma_load_3d(q_s + blk * (NR * 128), &tmq, q_ready, 0, row0, blk, policy_evict_last());
       }
       const int32_t* bt_row = P.block_tables + int64_t(it.b) * P.max_blocks_per_seq;
-      const int box_rows = bs < kTcTok ? bs : kTcTok;
+      // the largest power of two dividing both the block and the tile: a
+      // box never crosses a block (block_size 96 moves 32-token boxes)
+      const int box_rows = (bs & -bs) < kTcTok ? (bs & -bs) : kTcTok;
       const int pieces = kTcTok / box_rows;
       int issued = 0;
       bool ok = true;

@@ -17,6 +17,15 @@ pa_status validate_config(const pa_config* cfg);
 
 inline int64_t max_q(const pa_config& c) { return c.max_seqlen_q > 0 ? c.max_seqlen_q : 1; }
 
+// Tokens per TMA box of a kernel with `tile`-token key tiles (a power of two):
+// the largest power of two dividing both the block size and the tile, so that
+// no box crosses from one block into the next physical one. The kernels derive
+// the same figure from the block size.
+inline int box_tokens(int block_size, int tile) {
+  const int p2 = block_size & -block_size;
+  return p2 < tile ? p2 : tile;
+}
+
 // The host-side checks of pa_forward (configuration, pointers, alignment,
 // workspace size), done before anything is enqueued; the workspace pointer
 // itself is checked (non-null, 256-byte aligned) only with check_workspace.

@@ -167,7 +167,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_attn_kernel(
       const bool is_k = warp == 0;
       const uint64_t pol = policy_evict_last();  // every row tile of the sequence reads it
       const int32_t* bt_row = P.block_tables + int64_t(it.b) * P.max_blocks_per_seq;
-      const int box_rows = bs < kPfTok ? bs : kPfTok;
+      // the largest power of two dividing both the block and the tile: a
+      // box never crosses a block (block_size 48 moves 16-token boxes)
+      const int box_rows = (bs & -bs) < kPfTok ? (bs & -bs) : kPfTok;
       const int pieces = kPfTok / box_rows;
       // 64-dim blocks of this head in the map's rows (shared KV: V over the K rows)
       const int z0 = is_k ? it.kvh * H2 : it.kvh * ((P.kv_shared ? P.hk : HD) / 64);

@@ -249,6 +249,22 @@ TC_CASES = {
     "tc_hk576_two_heads": lambda: W.make_workload("tc576", context_lens=[300, 129], num_heads=32,
                                                   kv_heads=2, head_size_k=576, head_size_v=512,
                                                   block_size=128, std=0.5, seed=37),
+    # block sizes that neither divide nor are a multiple of the key tile: the
+    # boxes are the largest power of two dividing the block, so none crosses
+    # into the next physical block (64-token tiles: 48 -> 16, 96 -> 32;
+    # 128-token tiles: 80 -> 16, 48 -> 16)
+    "tc_bs48": lambda: W.make_workload("tc48", context_lens=[300, 1000, 47], num_heads=16,
+                                       kv_heads=1, head_size_k=128, block_size=48, seed=45,
+                                       chunk_blocks=5),
+    "tc_bs96_g64": lambda: W.make_workload("tc96", context_lens=[500, 97], num_heads=64,
+                                           kv_heads=1, head_size_k=128, block_size=96, seed=46),
+    "pf_bs80": lambda: W.make_workload("pf80", context_lens=[400, 250], q_seqlens=[16, 12],
+                                       num_heads=8, kv_heads=1, head_size_k=128, block_size=80,
+                                       mask_type=W.MASK_NORM_COMPRESS, seed=47),
+    "pf_pair_bs48": lambda: W.make_workload("pp48", context_lens=[700, 330], q_seqlens=[300, 330],
+                                            num_heads=4, kv_heads=2, head_size_k=128,
+                                            block_size=48, mask_type=W.MASK_NORM_COMPRESS,
+                                            seed=48),
     # 576/512 shared with 16-token blocks: the half slot moves as one box per block
     "tc_mla_bs16": lambda: W.make_workload("mla16", context_lens=[200, 33], num_heads=64,
                                            kv_heads=1, head_size_k=576, head_size_v=512,
