@@ -98,6 +98,7 @@ KERNEL_SOURCES = {
     "mma_decode_kernel": ["pa_decode_mma.cuh", "pa_decode_mma.cu"],
     "fma_decode_kernel": ["pa_decode_fma.cuh"],
     "tc_decode_kernel": ["pa_decode_tc.cuh", "pa_decode_tc.cu"],
+    "wide_decode_kernel": ["pa_decode_wide.cuh", "pa_decode_wide.cu", "pa_decode_mma.cuh"],
     "pf_attn_kernel": ["pa_prefill_tc.cuh", "pa_prefill_tc.cu", "pa_decode_tc.cuh"],
     "pf_pair_kernel": ["pa_prefill_pair.cuh", "pa_prefill_pair.cu", "pa_prefill_tc.cuh",
                        "pa_decode_tc.cuh"],
@@ -128,11 +129,16 @@ def ncu_traffic(kernel: str, workload: str):
     return float(m_b.group(1))
 
 
-def dominant_kernel(cfg):
-    """The attention kernel pa_forward picks for this configuration."""
+def dominant_kernel(cfg, shared_kv=False):
+    """The attention kernel pa_forward picks for this configuration (shared_kv:
+    value_cache is key_cache)."""
     rows = (cfg.num_heads // cfg.kv_heads) * max(1, cfg.max_seqlen_q)
     if rows > 64 and cfg.head_size_k == cfg.head_size_v and cfg.head_size_k in (64, 128):
         return "pf_pair_kernel" if rows > 128 else "pf_attn_kernel"
+    hk, hv = cfg.head_size_k, cfg.head_size_v
+    wide = shared_kv and ((hk, hv) == (576, 512) or (hk == hv and hk in (256, 512)))
+    if 8 < rows <= 16 and wide:
+        return "wide_decode_kernel"
     if rows > 8:
         return "tc_decode_kernel"
     mma = (cfg.head_size_k == cfg.head_size_v and cfg.head_size_k in (64, 128, 256, 512)) or \
@@ -494,7 +500,7 @@ def measure(name, args, steps, dev, stream, flush, rank, peaks_, read_gbs, cpu_s
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "bytes": "KV + Q + O per launch (algorithmic)", "frac": achieved / peak,
                 "read_peak": read_gbs, "frac_read": achieved / read_gbs if read_gbs else None}
-    kernel = dominant_kernel(db.cfg)
+    kernel = dominant_kernel(db.cfg, w.shared_kv)
     base = None
     if not args.no_cpu_baseline and world == 1:
         base = cpu_baseline(w, cpu_seconds)

@@ -13,6 +13,7 @@
 #include "pa_testing.h"
 #include "pa_combine.cuh"
 #include "pa_decode_mma.cuh"
+#include "pa_decode_wide.cuh"
 #include "pa_decode_tc.cuh"
 #include "pa_prefill_pair.cuh"
 #include "pa_prefill_tc.cuh"
@@ -306,6 +307,14 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
       return PA_ERR_CUDA;
     err = TR == PA_PF_PAIR_ROWS ? launch_pf_pair(tmk, tmv, P, n_items, stream)
                                 : launch_pf(tmk, tmv, P, n_items, stream);
+  } else if (tc_tile_rows(P.group, P.mask_q) == 16 && wide_supported(hk, hv, kv_shared)) {
+    // 9-16 rows over a shared-KV cache: the 16-row warp-level MMA kernel,
+    // 64-token tiles of every 64-dim block in one box (64-token boxes), else
+    // one box per block piece and 64-dim block
+    const int rows = box_tokens(c.block_size, 64);
+    CUtensorMap tmk;
+    if (!cache_map_3d(&tmk, key_cache, c, hk, rows, rows == 64 ? hk / 64 : 1)) return PA_ERR_CUDA;
+    err = launch_wide(tmk, P, n_items, stream);
   } else {
     // 64-row tiles on the tcgen05 kernel: boxes of the largest power of two
     // (at most 64) dividing the block size

@@ -237,26 +237,12 @@ __device__ __forceinline__ bool softmax_bar_or(bool pred) {
   return r != 0;
 }
 
-// Maximum over the warp (redux.sync, float form of sm_100 and later).
-__device__ __forceinline__ float warp_max(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
-
 // Lane 0 waits; the whole warp gets its verdict.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane,
                                           long long limit = kWaitLimitCycles) {
   bool ok = true;
   if (lane == 0) ok = mbar_wait(bar, parity, limit);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-}
-
-// Sum over the warp.
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
 }
 
 template <int HK, int HV, int NR, bool SH>

@@ -16,7 +16,7 @@ EXPECTED = {
     "spec_decode": "mma_decode_kernel",      # 4 rows (q = 4)
     "alibi_decode": "fma_decode_kernel",     # 1 row
     "mqa_split": "tc_decode_kernel",         # 64 rows, 512 dims
-    "mla_decode": "tc_decode_kernel",        # 16 rows, 576/512
+    "mla_decode": "wide_decode_kernel",      # 16 rows over a shared 576/512 cache
     "prefill_causal": "pf_pair_kernel",      # 2048 rows -> 256-row tiles
 }
 
@@ -43,7 +43,7 @@ def _light(name):
 @pytest.mark.parametrize("name", sorted(EXPECTED))
 def test_dominant_kernel_matches_dispatch(lib, name):
     cfg = _light(name)
-    assert bench.dominant_kernel(cfg) == EXPECTED[name]
+    assert bench.dominant_kernel(cfg, name == "mla_decode") == EXPECTED[name]
     # the tile height the planner uses agrees with that kernel's row range
     L = 2048 if cfg.max_seqlen_q > 1 else 300
     ql = np.array([cfg.max_seqlen_q] * 2, np.int32) if cfg.max_seqlen_q > 1 else None
@@ -51,6 +51,7 @@ def test_dominant_kernel_matches_dispatch(lib, name):
     tile = int((p.work[:, 3] - p.work[:, 2]).max())
     rows = (cfg.num_heads // cfg.kv_heads) * cfg.max_seqlen_q
     want = {"fma_decode_kernel": rows, "mma_decode_kernel": rows, "tc_decode_kernel": min(64, rows),
+            "wide_decode_kernel": rows,
             "pf_attn_kernel": 128, "pf_pair_kernel": 256}[EXPECTED[name]]
     assert tile == want
     # every kernel named has its device sources listed for the profile check

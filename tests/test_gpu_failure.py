@@ -52,6 +52,10 @@ CASES = {
     "tc_r16_bs16": (lambda: W.make_workload("r16", context_lens=[100, 300, 17, 129],
                                             num_heads=16, kv_heads=1, head_size_k=128,
                                             block_size=16, seed=62), 2),
+    # 16-row warp-level MMA kernel, shared 576/512 cache, split items
+    "wide_mla": (lambda: W.make_workload("wmla", context_lens=[900, 300, 65], num_heads=16,
+                                         kv_heads=1, head_size_k=576, head_size_v=512,
+                                         block_size=64, std=0.5, seed=64, shared_kv=True), 4),
     # tcgen05 kernel, 64 rows of a 512-dim MQA head
     "tc_mqa_hd512": (lambda: W.make_workload("mqa", context_lens=[1500, 700], num_heads=64,
                                              kv_heads=1, head_size_k=512, block_size=128,

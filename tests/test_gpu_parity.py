@@ -239,6 +239,37 @@ TC_CASES = {
     "tc_norm": lambda: W.make_workload("tcn", context_lens=[300, 1200], q_seqlens=[2, 1],
                                        num_heads=16, kv_heads=1, head_size_k=128, block_size=64,
                                        mask_type=W.MASK_NORM, seed=39, chunk_blocks=6),
+    # 16-row tcgen05 tiles of 256/512-dim heads with separate caches:
+    # 12 rows, 256-dim heads, ALiBi, 32-token blocks
+    "tc_r12_hd256_alibi": lambda: W.make_workload("w256", context_lens=[333, 1000, 17], num_heads=24,
+                                                kv_heads=2, head_size_k=256, block_size=32,
+                                                mask_type=W.MASK_ALIBI, seed=49, chunk_blocks=3),
+    # 8 heads x 2 tokens, 512-dim heads, MASK_TYPE_NORM, 16-token blocks
+    "tc_r16_hd512_norm_q2": lambda: W.make_workload("w512", context_lens=[300, 90], q_seqlens=[2, 1],
+                                                  num_heads=8, kv_heads=1, head_size_k=512,
+                                                  block_size=16, std=0.5, mask_type=W.MASK_NORM,
+                                                  seed=50, chunk_blocks=7),
+    # 9-16 rows over a shared-KV cache run on the 16-row warp-level MMA kernel:
+    # hk = hv = 512 shared, 16 rows, 32-token blocks (two pieces a tile)
+    "wide_hd512_shared": lambda: W.make_workload("ws512", context_lens=[777, 64, 1], num_heads=16,
+                                                 kv_heads=1, head_size_k=512, block_size=32,
+                                                 std=0.5, seed=53, shared_kv=True, chunk_blocks=5),
+    # hk = hv = 256 shared, 12 rows of two kv heads, ALiBi, 128-token blocks
+    "wide_hd256_shared_alibi": lambda: W.make_workload("ws256", context_lens=[1000, 200], num_heads=24,
+                                                       kv_heads=2, head_size_k=256, block_size=128,
+                                                       mask_type=W.MASK_ALIBI, seed=54,
+                                                       shared_kv=True, chunk_blocks=3),
+    # 4 heads x 4 tokens of the shared latent cache, compressed causal mask past
+    # 2048 keys (sigma > 0), 48-token blocks
+    "wide_mla_causal_bs48": lambda: W.make_workload("wmc", context_lens=[2500, 70], q_seqlens=4,
+                                                    num_heads=4, kv_heads=1, head_size_k=576,
+                                                    head_size_v=512, block_size=48, std=0.5,
+                                                    mask_type=W.MASK_NORM_COMPRESS, seed=51,
+                                                    shared_kv=True, chunk_blocks=9),
+    # 16 rows, shared latent cache, 96-token blocks (32-token boxes), one short sequence
+    "wide_mla_bs96": lambda: W.make_workload("wm96", context_lens=[1000, 5], num_heads=16,
+                                             kv_heads=1, head_size_k=576, head_size_v=512,
+                                             block_size=96, std=0.5, seed=52, shared_kv=True),
     # MLA-style shared-KV cache: K rows of 576 dims, V = their first 512
     "tc_mla_shared": lambda: W.make_workload("mla", context_lens=[700, 1500, 65], num_heads=16,
                                              kv_heads=1, head_size_k=576, head_size_v=512,
