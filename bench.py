@@ -3,10 +3,12 @@
 One step is one pass of the whole device path over one synthetic batch:
 pa_forward over the planned work list (the attention kernel, then the split-KV
 combine kernel when the plan has split tiles). The work list comes from
-pa_plan before the timed region (host code, timed separately as plan_us). The end-to-end number (`e2e`) starts from
-pinned host buffers: each timed step replays one recorded CUDA graph that
-copies the step's inputs to the device, plans on the device, runs attention
-and copies the output back, and the host waits for it. The same step planned
+pa_plan before the timed region (host code, timed separately as plan_us).
+The end-to-end number (`e2e`) starts from pinned host buffers: each timed
+step replays one recorded CUDA graph that copies the step's inputs to the
+device, plans on the device and runs attention, whose kernels store the
+output straight into a pinned host tensor (device-to-host bytes counted as
+the output's size), and the host waits for it. The same step planned
 on the host with direct launches is reported beside it (`e2e.host_planned`),
 and the graph's stages are timed one by one with CUDA events
 (`e2e.breakdown_us`).
@@ -429,8 +431,9 @@ def measure(name, args, steps, dev, stream, flush, rank, peaks_, read_gbs, cpu_s
         kernel_ms = statistics.mean(times)
 
     # end to end through the C ABI with host buffers: GraphStep replays one
-    # graph per step (copy in, device plan, attention, copy out; the host
-    # waits); HostStep plans on the host and launches directly; the graph's
+    # graph per step (copy in, device plan, attention storing the output into
+    # pinned host memory; the host waits); HostStep plans on the host and
+    # launches directly; the graph's
     # stages are also run directly with events between them
     def fill(st_):
         st_.query.copy_(torch.from_numpy(np.ascontiguousarray(w.query)))
@@ -462,14 +465,14 @@ def measure(name, args, steps, dev, stream, flush, rank, peaks_, read_gbs, cpu_s
     # the stages queue up behind the L2 flush (the step's stream waits for the
     # flush's), so the events measure the GPU's time on each stage rather
     # than the host's time to enqueue the next one
-    stage_ms = [[] for _ in range(4)]
+    stage_ms = [[] for _ in range(3)]
     for _ in range(max(1, args.e2e_steps // 2)):
         torch.cuda.synchronize()
         flush_l2(flush)
         gs.stream.wait_stream(torch.cuda.current_stream(dev))
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         gs.run_stages(ev)
-        for k in range(4):
+        for k in range(3):
             stage_ms[k].append(ev[k].elapsed_time(ev[k + 1]))
     if e2e_t:
         for what, s_ in (("graph", gs.status()), ("host-planned", hs.status(stream))):
@@ -528,10 +531,10 @@ def measure(name, args, steps, dev, stream, flush, rank, peaks_, read_gbs, cpu_s
             "d2h_bytes_per_step": int(gs.out.numel() * gs.out.element_size()),
             "ms_per_step": e2e_all * 1e3,
             "path": "GraphStep: one graph replay per step (device plan reading the lengths "
-                    "from pinned host memory, beside the copy of the inputs; attention, "
-                    "combine, copy out), host waits",
+                    "from pinned host memory, beside the copy of the inputs; attention and "
+                    "combine storing the output straight into pinned host memory), host waits",
             "breakdown_us": {"h2d_copy": stages[0], "plan_device": stages[1],
-                             "attention": stages[2], "d2h_copy": stages[3],
+                             "attention_and_d2h": stages[2],
                              "how": "the graph's stages enqueued one after another (the whole "
                                     "arena copied first, no overlap) on its stream behind the L2 "
                                     "flush, CUDA events between them"},

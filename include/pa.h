@@ -224,9 +224,8 @@ pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens, const int32
  *               one cache whose K row also carries V, V_b[j] being the first
  *               hv dims of K_b[j] (the latent cache of MLA-style models, K of
  *               576 dims and V of 512 in the head-size rule of the
- *               "Constraints" page). The CUDA-core and mma.sync kernels then
- *               fetch each row once; the tensor-core kernel reads the V dims
- *               of a row a second time, normally from L2.
+ *               "Constraints" page). Every kernel then fetches each row once
+ *               and reads V from the K rows it already holds.
  * block_tables  device int32 [batch, max_blocks_per_seq]
  * context_lens  device int32 [batch]
  * q_seqlens     device int32 [batch], or NULL when every q_b = 1
@@ -238,7 +237,10 @@ pa_status pa_plan(const pa_config* cfg, const int32_t* context_lens, const int32
  * workspace     device, >= pa_plan's workspace_bytes, 256-byte aligned; its
  *               status word must be zero before the first call (see
  *               pa_status_clear) and is only ever OR-ed by the kernels
- * out           device fp16 [sum q_b, H, hv]
+ * out           fp16 [sum q_b, H, hv], 16-byte aligned: device memory, or
+ *               pinned host memory mapped into the device's address space
+ *               (the kernels then store the result straight into host
+ *               memory, with no copy afterwards)
  * stream        a cudaStream_t (NULL = legacy default stream)
  *
  * Host-side errors return before anything is enqueued. Block-table entries
