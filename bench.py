@@ -6,9 +6,10 @@ combine kernel when the plan has split tiles). The work list comes from
 pa_plan before the timed region (host code, timed separately as plan_us).
 The end-to-end number (`e2e`) starts from pinned host buffers: each timed
 step replays one recorded CUDA graph that copies the step's inputs to the
-device, plans on the device and runs attention, whose kernels store the
-output straight into a pinned host tensor (device-to-host bytes counted as
-the output's size), and the host waits for it. The same step planned
+device, plans on the device and runs attention, whose kernels store an
+output of up to 4 MiB straight into a pinned host tensor (a larger one is
+copied back from device memory; device-to-host bytes are the output's size
+either way), and the host waits for it. The same step planned
 on the host with direct launches is reported beside it (`e2e.host_planned`),
 and the graph's stages are timed one by one with CUDA events
 (`e2e.breakdown_us`).
@@ -465,14 +466,14 @@ def measure(name, args, steps, dev, stream, flush, rank, peaks_, read_gbs, cpu_s
     # the stages queue up behind the L2 flush (the step's stream waits for the
     # flush's), so the events measure the GPU's time on each stage rather
     # than the host's time to enqueue the next one
-    stage_ms = [[] for _ in range(3)]
+    stage_ms = [[] for _ in range(4)]
     for _ in range(max(1, args.e2e_steps // 2)):
         torch.cuda.synchronize()
         flush_l2(flush)
         gs.stream.wait_stream(torch.cuda.current_stream(dev))
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         gs.run_stages(ev)
-        for k in range(3):
+        for k in range(4):
             stage_ms[k].append(ev[k].elapsed_time(ev[k + 1]))
     if e2e_t:
         for what, s_ in (("graph", gs.status()), ("host-planned", hs.status(stream))):
@@ -532,9 +533,11 @@ def measure(name, args, steps, dev, stream, flush, rank, peaks_, read_gbs, cpu_s
             "ms_per_step": e2e_all * 1e3,
             "path": "GraphStep: one graph replay per step (device plan reading the lengths "
                     "from pinned host memory, beside the copy of the inputs; attention and "
-                    "combine storing the output straight into pinned host memory), host waits",
+                    "combine storing an output of at most 4 MiB straight into pinned host "
+                    "memory, a larger one into device memory, then copied), host waits",
+            "out_to_host": "kernels write pinned memory" if gs.d_out is None else "copy",
             "breakdown_us": {"h2d_copy": stages[0], "plan_device": stages[1],
-                             "attention_and_d2h": stages[2],
+                             "attention": stages[2], "d2h_copy": stages[3],
                              "how": "the graph's stages enqueued one after another (the whole "
                                     "arena copied first, no overlap) on its stream behind the L2 "
                                     "flush, CUDA events between them"},

@@ -330,6 +330,22 @@ def list_capacity(cfg: pa_config) -> tuple[int, int]:
     return items, tiles
 
 
+# Outputs up to this size are stored by the kernels straight into pinned host
+# memory (no copy node: about 10 us less per step for a decode batch); larger
+# ones go to a device buffer and one copy, since the kernels' scattered stores
+# over the host link are slower than the copy engine at volume (a 67 MB
+# prefill output took 1.7 ms that way, against 0.35 ms for the copy).
+ZERO_COPY_OUT_BYTES = 4 << 20
+
+
+def _device_out(out, dev):
+    """A device buffer for ``out``, or None when the kernels write it directly."""
+    import torch
+    if out.numel() * out.element_size() <= ZERO_COPY_OUT_BYTES:
+        return None
+    return torch.empty(out.shape, dtype=out.dtype, device=dev)
+
+
 class HostStep:
     """One attention step whose per-step inputs live in pinned host memory.
 
@@ -338,10 +354,11 @@ class HostStep:
     ``context_lens`` and ``q_seqlens``; :meth:`run` then plans the step
     (pa_plan, writing the work and combine lists straight into the same pinned
     arena), moves the used part of the arena to the device with one
-    host-to-device copy, enqueues pa_forward on device pointers into it, with
-    the pinned ``out`` tensor as its output (the kernels store the result
-    straight into host memory), and waits for the stream. The KV cache, mask
-    and ALiBi slopes stay resident on the device.
+    host-to-device copy, enqueues pa_forward on device pointers into it and
+    waits for the stream. An output of at most ``ZERO_COPY_OUT_BYTES`` is
+    stored by the kernels straight into the pinned ``out`` tensor; a larger
+    one goes to a device buffer and is copied back. The KV cache, mask and
+    ALiBi slopes stay resident on the device.
     """
 
     def __init__(self, cfg: pa_config, key_cache, value_cache, total_q: int, mask=None,
@@ -381,6 +398,7 @@ class HostStep:
         self.context_lens = hview("context_lens", torch.int32, (B,))
         self.q_seqlens = hview("q_seqlens", torch.int32, (B,)) if has_ql else None
         self.out = torch.empty((self.total_q, H, hv), dtype=torch.float16).pin_memory()
+        self.d_out = _device_out(self.out, dev)
         self._d = {k: self.d_arena.data_ptr() + v for k, v in self.offsets.items()}
         self._h = {k: self.h_arena.data_ptr() + v for k, v in self.offsets.items()}
         self.workspace = None
@@ -388,7 +406,8 @@ class HostStep:
         self.n_items = self.n_combine = 0
 
     def run(self, stream=None):
-        """Plan, copy in, attend into the pinned ``out`` tensor; returns it."""
+        """Plan, copy in, attend (into the pinned ``out`` tensor, or a device
+        buffer copied into it); returns ``out``."""
         import torch
         lib = load_library()
         cfg, h, d, P = self.cfg, self._h, self._d, ctypes.c_void_p
@@ -412,9 +431,13 @@ class HostStep:
                             P(d["q_seqlens"]) if has_ql else None, _tptr(self.mask),
                             _tptr(self.alibi_slopes), P(d["work"]), self.n_items,
                             P(d["combine"]) if self.n_combine else None, self.n_combine,
-                            _tptr(self.workspace), self.workspace.numel(), _tptr(self.out),
+                            _tptr(self.workspace), self.workspace.numel(),
+                            _tptr(self.out if self.d_out is None else self.d_out),
                             ctypes.c_void_p(s.cuda_stream))
         _check(st, "pa_forward")
+        if self.d_out is not None:
+            with torch.cuda.stream(s):
+                self.out.copy_(self.d_out, non_blocking=True)
         s.synchronize()
         return self.out
 
@@ -483,9 +506,10 @@ class GraphStep:
     arena (mapped into the device's address space), beside it on a second
     stream the host-to-device copy of the arena, then the forward pass over
     the planner's lists (pa_forward_device_plan), whose output is the pinned
-    ``out`` tensor itself (the kernels store the result straight into host
-    memory). :meth:`run` replays it and waits, so a decode loop costs one
-    graph launch per step.
+    ``out`` tensor itself when it is at most ``ZERO_COPY_OUT_BYTES`` (the
+    kernels store the result straight into host memory), else a device buffer
+    copied into ``out``. :meth:`run` replays it and waits, so a decode loop
+    costs one graph launch per step.
     The launches do not depend on the lengths (grids are pa_plan_bounds'
     capacities), which is what allows the recording.
     """
@@ -530,8 +554,8 @@ class GraphStep:
                                    device=dev)
         self.counts = torch.zeros(PA_PLAN_COUNTS, dtype=torch.int32, device=dev)
         self.workspace = torch.zeros(max(ws, PA_STATUS_BYTES), dtype=torch.uint8, device=dev)
-        # the forward pass writes the output straight into this pinned tensor
         self.out = torch.empty((self.total_q, H, hv), dtype=torch.float16).pin_memory()
+        self.d_out = _device_out(self.out, dev)
         self.h2d_bytes = self.arena_bytes
         self.stream = torch.cuda.Stream(device=dev)
         self.side_stream = torch.cuda.Stream(device=dev)
@@ -541,10 +565,10 @@ class GraphStep:
         """Enqueue the step on its stream. Without ``events`` (the recorded
         graph), the copy of the query and block tables runs on a second stream
         beside the device planner, which needs only the lengths. With
-        ``events`` (four CUDA events) the stages run one after another, an event
+        ``events`` (five CUDA events) the stages run one after another, an event
         recorded before the host-to-device copy and after each stage (copy in,
-        device planner, attention and combine writing the output into pinned
-        host memory), to time them separately."""
+        device planner, attention and combine, copy out: empty when the kernels
+        write the pinned output themselves), to time them separately."""
         import torch
         lib, cfg, s = load_library(), self.cfg, self.stream
 
@@ -580,8 +604,13 @@ class GraphStep:
             _tptr(self._dbt), _tptr(self._dcl), _tptr(self._dql), _tptr(self.mask),
             _tptr(self.alibi_slopes), _tptr(self.work), self.work_cap, _tptr(self.combine),
             self.comb_cap, _tptr(self.counts), _tptr(self.workspace), self.workspace.numel(),
-            _tptr(self.out), ctypes.c_void_p(s.cuda_stream)), "pa_forward_device_plan")
+            _tptr(self.out if self.d_out is None else self.d_out),
+            ctypes.c_void_p(s.cuda_stream)), "pa_forward_device_plan")
         mark(3)
+        if self.d_out is not None:
+            with torch.cuda.stream(s):
+                self.out.copy_(self.d_out, non_blocking=True)
+        mark(4)
 
     def record(self):
         """Run the step once directly (kernel attributes and tensor maps are set
@@ -595,7 +624,7 @@ class GraphStep:
         self.graph = g
 
     def run_stages(self, events):
-        """Run the step's stages directly (no graph), recording ``events`` (four
+        """Run the step's stages directly (no graph), recording ``events`` (five
         CUDA events) around them for timing each stage, and wait."""
         self._enqueue(events)
         self.stream.synchronize()
