@@ -278,13 +278,20 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
   cudaError_t err;
   if (TR <= PA_FMA_MAX_ROWS) {
     const bool wide = (hk % 64 == 0) && (hv % 64 == 0);
-    const BoxGeom kg = box_geom(wide), vg = box_geom(wide);
     CUtensorMap tmk, tmv;
     // (with a shared-KV cache the warp kernels read V from the K boxes; the
     // V map is then built over the K rows and left unused)
-    if (!cache_map(&tmk, key_cache, c, hk, 16, kg) ||
-        !cache_map(&tmv, value_cache, c, kv_shared ? hk : hv, 16, vg))
-      return PA_ERR_CUDA;
+    if (wide) {
+      // one 3-D box per 16-token sub-tile: every 64-dim block of the head
+      if (!cache_map_3d(&tmk, key_cache, c, hk, 16, hk / 64) ||
+          !cache_map_3d(&tmv, value_cache, c, kv_shared ? hk : hv, 16, hv / 64))
+        return PA_ERR_CUDA;
+    } else {
+      const BoxGeom g = box_geom(false);
+      if (!cache_map(&tmk, key_cache, c, hk, 16, g) ||
+          !cache_map(&tmv, value_cache, c, kv_shared ? hk : hv, 16, g))
+        return PA_ERR_CUDA;
+    }
     if (TR >= 2 && mma_supported(hk, hv)) {
       err = launch_mma(tmk, tmv, P, n_items, stream);
     } else switch (TR) {

@@ -159,11 +159,19 @@ struct WarpPipe {
       const int row = phys * bs + off;
       uint8_t* dst = kbuf(n);
       mbar_arrive_expect_tx(bar, tile_bytes);
-      for (int j = 0; j < nkbox; ++j)
-        tma_load_2d(dst + j * kBoxBytes, tmk, bar, kvh * hk + j * KBW, row, pol);
-      if (!shared)
-        for (int j = 0; j < nvbox; ++j)
-          tma_load_2d(dst + v_off + j * vBoxBytes, tmv, bar, kvh * hv + j * VBW, row, pol);
+      if constexpr (KBW == 64 && VBW == 64) {
+        // 64-dim blocks: one 3-D box per sub-tile and cache, landing as the
+        // same [block][16 tokens][128 B] sequence the 2-D boxes would (fewer,
+        // larger copies: each costs the issuing lane time on a busy SM)
+        tma_load_3d(dst, tmk, bar, 0, row, kvh * nkbox, pol);
+        if (!shared) tma_load_3d(dst + v_off, tmv, bar, 0, row, kvh * nvbox, pol);
+      } else {
+        for (int j = 0; j < nkbox; ++j)
+          tma_load_2d(dst + j * kBoxBytes, tmk, bar, kvh * hk + j * KBW, row, pol);
+        if (!shared)
+          for (int j = 0; j < nvbox; ++j)
+            tma_load_2d(dst + v_off + j * vBoxBytes, tmv, bar, kvh * hv + j * VBW, row, pol);
+      }
     }
   }
 
