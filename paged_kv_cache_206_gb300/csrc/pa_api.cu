@@ -163,9 +163,10 @@ bool cache_map_3d(CUtensorMap* m, const void* base, const pa_config& c, int hs, 
 // The query [batch, H, hk] of a launch with one query token per sequence, as a
 // 3-D tensor for the tcgen05 kernel: dims (64 elements of a head-dim block,
 // batch * H rows, hk / 64 blocks), strides (row stride hk * 2 bytes, 128); a
-// box is G rows (the heads of one kv head, consecutive in memory) of one
-// 64-dim block, landing as [G][128 B] with the 128-byte swizzle.
-bool query_map(CUtensorMap* m, const void* query, const pa_config& c) {
+// box is G rows (the heads of one kv head, consecutive in memory) of
+// `blocks_per_box` 64-dim blocks, landing as [block][G][128 B] with the
+// 128-byte swizzle.
+bool query_map(CUtensorMap* m, const void* query, const pa_config& c, int blocks_per_box) {
   MapKey k{};
   k.base = query;
   k.rank = 3;
@@ -175,7 +176,7 @@ bool query_map(CUtensorMap* m, const void* query, const pa_config& c) {
   k.dims[2] = uint64_t(c.head_size_k / 64);
   k.box[0] = 64;
   k.box[1] = uint32_t(c.num_heads / c.kv_heads);
-  k.box[2] = 1;
+  k.box[2] = uint32_t(blocks_per_box);
   const cuuint64_t strides[2] = {cuuint64_t(c.head_size_k) * 2, 128};
   return cached_map(m, k, strides);
 }
@@ -338,8 +339,12 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
     P.q_tma = 0;
     tmq = tmk;
     if (max_q(c) == 1) {
-      if (!query_map(&tmq, query, c)) return PA_ERR_CUDA;
-      P.q_tma = 1;
+      // one box for the whole tile when its rows are exactly the group's
+      // (it lands as [block][G rows][128 B], the tile's layout), else one
+      // box per 64-dim block
+      const bool one_box = tc_tile_rows(P.group, P.mask_q) == P.group;
+      if (!query_map(&tmq, query, c, one_box ? hk / 64 : 1)) return PA_ERR_CUDA;
+      P.q_tma = one_box ? 2 : 1;
     }
     err = launch_tc(tmk, tmv, tmq, P, n_items, stream);
   }

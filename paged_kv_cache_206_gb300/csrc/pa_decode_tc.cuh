@@ -365,14 +365,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       if (is_k && P.q_tma) {
         // The query tile first, ahead of the K ring in the same queue: its G
         // rows (heads kvh * G .. of the sequence's one query token) are
-        // consecutive in the query; one box per 64-dim block, landing where
-        // the QK MMA reads it. Every split of the tile reads the same tile,
-        // so keep it in L2.
+        // consecutive in the query; one box per 64-dim block (q_tma 1), or
+        // one box of every block when the tile's rows are exactly the G
+        // (q_tma 2), landing where the QK MMA reads it. Every split of the
+        // tile reads the same tile, so keep it in L2.
         const int G = P.group;
         mbar_arrive_expect_tx(q_ready, uint32_t(KH) * G * 128);
         const int row0 = it.q_start * P.num_heads + it.kvh * G;
-        for (int blk = 0; blk < KH; ++blk)
-          tma_load_3d(q_s + blk * (NR * 128), &tmq, q_ready, 0, row0, blk, policy_evict_last());
+        if (P.q_tma == 2) {
+          tma_load_3d(q_s, &tmq, q_ready, 0, row0, 0, policy_evict_last());
+        } else {
+          for (int blk = 0; blk < KH; ++blk)
+            tma_load_3d(q_s + blk * (NR * 128), &tmq, q_ready, 0, row0, blk, policy_evict_last());
+        }
       }
       const int32_t* bt_row = P.block_tables + int64_t(it.b) * P.max_blocks_per_seq;
       // the largest power of two dividing both the block and the tile: a

@@ -229,7 +229,8 @@ struct FwdParams {
   int num_heads, kv_heads, group, hk, hv, block_size, max_blocks_per_seq, num_blocks;
   int mask_type;
   int kv_shared;     // V of a token = the first hv dims of its K row (value_cache == key_cache)
-  int q_tma;         // tcgen05 decode kernel: the query tile comes by TMA (tmq)
+  int q_tma;         // tcgen05 decode kernel: the query tile comes by TMA (tmq): 1 one box
+                     // per 64-dim block, 2 one box for the tile (its rows are exactly G)
   int mask_q;        // PA_MASK_NORM: mask is [batch][mask_q][mask_kv]
   int64_t mask_kv;
   float scale_log2;  // scale * log2(e)
