@@ -362,6 +362,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
       // 64-dim blocks per kv head in the map's rows: a shared-KV V map spans the K rows
       const int zbase = it.kvh * ((is_k || P.kv_shared ? HK : HV) / 64);
       const uint64_t pol = policy_evict_first();
+      // V copies start once the query tile has landed: the first QK (query
+      // and K tile 0) is then not queued behind every CTA's V ring
+      if (!is_k && P.q_tma && !mbar_wait(q_ready, 0, P.wait_limit)) set_status(P.status, PA_STATUS_BIT_TIMEOUT);
       if (is_k && P.q_tma) {
         // The query tile first, ahead of the K ring in the same queue: its G
         // rows (heads kvh * G .. of the sequence's one query token) are
