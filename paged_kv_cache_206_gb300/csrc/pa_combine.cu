@@ -14,9 +14,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   constexpr int kBatch = 16;  // splits whose partial rows a lane has in flight at once
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (C.counts && int(blockIdx.x) >= C.counts[1]) return;
-  // Launched as a programmatic dependent of the attention kernel: wait until
-  // that grid has finished and its partial results are visible.
-  grid_dependency_wait();
+  // The work and combine lists were complete before the attention kernel
+  // started: this entry and its first item are read while that kernel, whose
+  // programmatic dependent this is, still runs.
   const int32_t* e = C.combine + int64_t(blockIdx.x) * PA_COMBINE_INTS;
   const int kvh = e[1], first = e[2], S = e[3];
   const int32_t* item = C.work + int64_t(first) * PA_WORK_INTS;
@@ -28,6 +28,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   }
   const int rr = blockIdx.y * (kCombineThreads / 32) + warp;
   if (rr >= nrows) return;
+  // the partial results: wait until the attention grid has finished and its
+  // writes are visible
+  grid_dependency_wait();
   const float* lse = C.part_lse + slot0 + rr;  // split s at lse[s * nrows]
   // this warp's 128 dims (blockIdx.z), 4 a lane; split s at po[s * split_stride]
   const int d = blockIdx.z * 128 + lane * 4;
