@@ -302,16 +302,6 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
       case 4: err = launch_fma<4>(tmk, tmv, P, n_items, stream); break;
       default: err = launch_fma<8>(tmk, tmv, P, n_items, stream); break;
     }
-  } else if (TR == PA_PF_PAIR_ROWS && hk == 128 && hv == 128) {
-    // 256-row tiles of 128-dim heads: the two-SM kernel, each CTA of a pair
-    // staging 64 tokens of a K tile (both 64-dim halves in one box at 64-token
-    // boxes) and 128 tokens of one 64-dim half of V
-    const int krows = box_tokens(c.block_size, 64), vrows = box_tokens(c.block_size, 128);
-    CUtensorMap tmk, tmv;
-    if (!cache_map_3d(&tmk, key_cache, c, hk, krows, krows == 64 ? 2 : 1) ||
-        !cache_map_3d(&tmv, value_cache, c, kv_shared ? hk : hv, vrows, 1))
-      return PA_ERR_CUDA;
-    err = launch_pf_duo(tmk, tmv, P, n_items, stream);
   } else if (TR == PA_PF_TILE_ROWS || TR == PA_PF_PAIR_ROWS) {
     // rows meet many keys (more than one 64-row tile per kv head: 128-row
     // tiles, or 256-row tiles of two query tiles for prefill): 128-token key

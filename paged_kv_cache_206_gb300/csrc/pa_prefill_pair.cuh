@@ -573,9 +573,4 @@ __global__ void __launch_bounds__(kPpThreads, 1) pf_pair_kernel(
 cudaError_t launch_pf_pair(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdParams& P,
                            int64_t n_items, cudaStream_t stream);
 
-// The same tiles with 128-dim heads on pairs of SMs (pa_prefill_duo.cuh): a
-// cluster of two CTAs per work item.
-cudaError_t launch_pf_duo(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdParams& P,
-                          int64_t n_items, cudaStream_t stream);
-
 }  // namespace pa
