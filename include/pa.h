@@ -190,9 +190,10 @@ typedef struct pa_config {
  *   [0] b   [1] kvh   [2] first_item (index of split 0's item)   [3] S_b
  *
  * Workspace. PA_STATUS_BYTES of status first (word 0 collects PA_STATUS_BIT_*
- * flags), then P * hv fp32 partial outputs (already divided by their softmax
- * sum), then P fp32 log-sum-exps in natural-log units, where P is the number
- * of partial rows; each part starts on a 256-byte boundary.
+ * flags), then P * hv fp16 partial outputs (already divided by their softmax
+ * sum, so within the range of V), then P fp32 log-sum-exps in natural-log
+ * units, where P is the number of partial rows; each part starts on a
+ * 256-byte boundary.
  */
 #define PA_WORK_INTS 8
 #define PA_COMBINE_INTS 4

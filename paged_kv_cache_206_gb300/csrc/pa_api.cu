@@ -255,7 +255,7 @@ pa_status forward_impl(const pa_config* cfg, const void* query, const void* key_
   P.work = work;
   P.out = static_cast<__half*>(out);
   P.status = static_cast<uint32_t*>(workspace);
-  P.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.partial_o);
+  P.part_o = reinterpret_cast<__half*>(static_cast<char*>(workspace) + wl.partial_o);
   P.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.partial_lse);
   P.part_rows_cap = cap;
   P.num_heads = c.num_heads;

@@ -36,14 +36,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   const int d = blockIdx.z * 128 + lane * 4;
   const bool active = d < C.hv;
   const int64_t split_stride = int64_t(nrows) * C.hv;
-  const float* po = C.part_o + (int64_t(slot0) + rr) * C.hv + d;
+  const __half* po = C.part_o + (int64_t(slot0) + rr) * C.hv + d;
   // The first batch of partial rows is loaded together with the LSEs: one
   // round trip to L2 before the arithmetic, not one per pass.
-  float4 v[kBatch];
+  uint2 v[kBatch];  // four fp16 dims of split k
 #pragma unroll
   for (int k = 0; k < kBatch; ++k)
-    v[k] = (k < S && active) ? __ldg(reinterpret_cast<const float4*>(po + k * split_stride))
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[k] = (k < S && active) ? __ldg(reinterpret_cast<const uint2*>(po + k * split_stride))
+                             : make_uint2(0u, 0u);
   float M = -INFINITY;
   for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldg(lse + int64_t(s) * nrows));
 #pragma unroll
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
         if (s0 + k < S && active)
-          v[k] = __ldg(reinterpret_cast<const float4*>(po + (s0 + k) * split_stride));
+          v[k] = __ldg(reinterpret_cast<const uint2*>(po + (s0 + k) * split_stride));
     }
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
@@ -70,10 +70,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
       if (s >= S) break;
       const float w = s < 32 ? __shfl_sync(0xffffffffu, w_lane, s)
                              : __expf(__ldg(lse + int64_t(s) * nrows) - M);
-      acc.x += w * v[k].x;
-      acc.y += w * v[k].y;
-      acc.z += w * v[k].z;
-      acc.w += w * v[k].w;
+      const float2 lo = h2f2(v[k].x), hi = h2f2(v[k].y);
+      acc.x += w * lo.x;
+      acc.y += w * lo.y;
+      acc.z += w * hi.x;
+      acc.w += w * hi.y;
     }
   }
   if (active) {

@@ -14,7 +14,7 @@ constexpr int kCombineThreads = 256;     // 8 warps, one row each
 struct CombineParams {
   const int32_t* combine;
   const int32_t* work;
-  const float* part_o;
+  const __half* part_o;
   const float* part_lse;
   __half* out;
   uint32_t* status;

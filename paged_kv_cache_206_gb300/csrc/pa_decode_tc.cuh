@@ -866,10 +866,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
         tmem_wait_ld();
         if (!fits) continue;
         if (partial) {
-          float* dst = P.part_o + (int64_t(it.slot) + rbase) * HV + d;
+          // Lanes 2k and 2k + 1 hold dims d and d + 1: each stores both (one
+          // half2) for half of the 32 rows, the even lane rows rbase + i, the
+          // odd lane rows rbase + RH/2 + i, taking the partner's value by
+          // shuffle (128 bytes a warp store, as many bytes as an fp32 row)
+          const bool odd = lane & 1;
+          __half2* dst = reinterpret_cast<__half2*>(
+              P.part_o + (int64_t(it.slot) + rbase + (odd ? RH / 2 : 0)) * HV + (d & ~1));
 #pragma unroll
-          for (int i = 0; i < RH; ++i)
-            if (rbase + i < it.nrows) dst[int64_t(i) * HV] = o[i] * inv_l[rbase + i];
+          for (int i = 0; i < RH / 2; ++i) {
+            const float lo = o[i] * inv_l[rbase + i];
+            const float hi = o[RH / 2 + i] * inv_l[rbase + RH / 2 + i];
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+            const float keep = odd ? hi : lo;
+            const int row = rbase + (odd ? RH / 2 : 0) + i;
+            if (row < it.nrows)
+              dst[int64_t(i) * (HV / 2)] = odd ? __floats2half2_rn(got, keep) : __floats2half2_rn(keep, got);
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < RH; ++i)
@@ -880,7 +893,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_decode_kernel(
     } else if (done && it.slot >= 0 && int64_t(it.slot) + it.nrows <= P.part_rows_cap) {
       // an empty split (causal trim): weight zero in the combine
       for (int idx = t + 128 * rh; idx < it.nrows * HV; idx += 256) {
-        P.part_o[int64_t(it.slot) * HV + idx] = 0.f;
+        P.part_o[int64_t(it.slot) * HV + idx] = __float2half_rn(0.f);
         if (idx % HV == 0) P.part_lse[it.slot + idx / HV] = -INFINITY;
       }
     }

@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) wide_decode_kernel(
     // an empty split (causal trim): weight zero in the combine
     if (partial)
       for (int idx = tid; idx < it.nrows * HV; idx += NTH) {
-        P.part_o[int64_t(it.slot) * HV + idx] = 0.f;
+        P.part_o[int64_t(it.slot) * HV + idx] = __float2half_rn(0.f);
         if (idx % HV == 0) P.part_lse[it.slot + idx / HV] = -INFINITY;
       }
     return;
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) wide_decode_kernel(
         const int d = vd0 + mt * 16 + g + 8 * (e >> 1);
         const float val = o[mt][j][e] * inv[j][e & 1];
         if (partial) {
-          P.part_o[(int64_t(it.slot) + row) * HV + d] = val;
+          P.part_o[(int64_t(it.slot) + row) * HV + d] = __float2half_rn(val);
         } else {
           const int rr = it.r0 + row;
           P.out[(int64_t(it.q_start + rr / G) * P.num_heads + it.kvh * G + rr % G) * HV + d] =

@@ -223,7 +223,7 @@ struct FwdParams {
   const int32_t* counts;  // device plan: counts[0] items (CTAs past it exit), else null
   __half* out;
   uint32_t* status;
-  float* part_o;
+  __half* part_o;  // split items' rows, normalised, fp16
   float* part_lse;
   int64_t part_rows_cap;
   int num_heads, kv_heads, group, hk, hv, block_size, max_blocks_per_seq, num_blocks;

@@ -66,7 +66,7 @@ PA_HOST_DEVICE inline int64_t wave_fit_hi(int64_t c0, int64_t max_nb) {
 }
 
 struct WorkspaceLayout {
-  size_t partial_o;    // byte offset of the fp32 [P, hv] partial outputs
+  size_t partial_o;    // byte offset of the fp16 [P, hv] partial outputs
   size_t partial_lse;  // byte offset of the fp32 [P] log-sum-exps
   size_t total;        // bytes
 };
@@ -77,7 +77,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline WorkspaceLayout workspace_layout(int64_t partial_rows, int hv) {
   WorkspaceLayout w;
   w.partial_o = PA_STATUS_BYTES;
-  w.partial_lse = align256(w.partial_o + size_t(partial_rows) * size_t(hv) * 4);
+  w.partial_lse = align256(w.partial_o + size_t(partial_rows) * size_t(hv) * 2);
   w.total = align256(w.partial_lse + size_t(partial_rows) * 4);
   return w;
 }
@@ -86,7 +86,7 @@ inline WorkspaceLayout workspace_layout(int64_t partial_rows, int hv) {
 inline int64_t workspace_rows(size_t bytes, int hv) {
   if (bytes < PA_STATUS_BYTES) return -1;
   // largest P with workspace_layout(P, hv).total <= bytes
-  int64_t lo = 0, hi = int64_t((bytes - PA_STATUS_BYTES) / (size_t(hv) * 4 + 4)) + 1;
+  int64_t lo = 0, hi = int64_t((bytes - PA_STATUS_BYTES) / (size_t(hv) * 2 + 4)) + 1;
   while (lo + 1 < hi) {
     const int64_t mid = (lo + hi) / 2;
     if (workspace_layout(mid, hv).total <= bytes) lo = mid; else hi = mid;

@@ -535,9 +535,16 @@ __global__ void __launch_bounds__(kPpThreads, 1) pf_pair_kernel(
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = any ? o[i] * inv : 0.f;
         if (partial) {
-          float4* dst = reinterpret_cast<float4*>(P.part_o + (int64_t(it.slot) + r) * HD + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(P.part_o + (int64_t(it.slot) + r) * HD + c * 32);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          for (int i = 0; i < 4; ++i) {
+            uint4 pk;
+            pk.x = pack_half2(o[8 * i + 0], o[8 * i + 1]);
+            pk.y = pack_half2(o[8 * i + 2], o[8 * i + 3]);
+            pk.z = pack_half2(o[8 * i + 4], o[8 * i + 5]);
+            pk.w = pack_half2(o[8 * i + 6], o[8 * i + 7]);
+            dst[i] = pk;
+          }
         } else {
           uint4* dst = reinterpret_cast<uint4*>(
               P.out + (int64_t(it.q_start + qi) * P.num_heads + it.kvh * G + rr % G) * HD + c * 32);

@@ -203,8 +203,8 @@ struct WarpPipe {
 
 // Merge the per-warp softmax states (m, l in base 2; O unnormalised) stored at
 // `base` with stride merge_stride(RT, hv), and write the tile's rows: fp16
-// output when the item is unsplit, else fp32 partial rows and their natural-log
-// LSE. Called by the whole CTA after a __syncthreads.
+// output when the item is unsplit, else fp16 partial rows and their fp32
+// natural-log LSE. Called by the whole CTA after a __syncthreads.
 template <int RT>
 __device__ __forceinline__ void merge_store(const FwdParams& P, const Item& it, const float* base,
                                             int nw) {
@@ -231,7 +231,7 @@ __device__ __forceinline__ void merge_store(const FwdParams& P, const Item& it, 
       const int r = it.r0 + rr, i = r / G, h = it.kvh * G + r % G;
       P.out[(int64_t(it.q_start + i) * P.num_heads + h) * hv + d] = __float2half_rn(val);
     } else {
-      P.part_o[(int64_t(it.slot) + rr) * hv + d] = val;
+      P.part_o[(int64_t(it.slot) + rr) * hv + d] = __float2half_rn(val);
       if (d == 0) P.part_lse[it.slot + rr] = (M + log2f(lsum)) * kLn2;
     }
   }

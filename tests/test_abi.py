@@ -112,7 +112,7 @@ def test_plan_bounds_and_device_plan_host_checks(lib):
         rows = (c.num_heads // c.kv_heads) * max(1, c.max_seqlen_q)
         tr = rows if rows <= 8 else 64
         up = lambda x: (x + 255) // 256 * 256
-        assert ws == up(up(256 + w * tr * c.head_size_v * 4) + w * tr * 4)
+        assert ws == up(up(256 + w * tr * c.head_size_v * 2) + w * tr * 4)
     fake = ctypes.c_void_p(1 << 20)
     c = _cfg()
 

@@ -92,7 +92,7 @@ def test_device_plan_equals_host_plan(seed):
     assert np.array_equal(comb[:m], host.combine)
     # partial rows: the workspace pa_plan sizes holds exactly counts[2] rows
     up = lambda x: (x + 255) // 256 * 256
-    assert host.workspace_bytes == up(up(256 + int(counts[2]) * cfg.head_size_v * 4) +
+    assert host.workspace_bytes == up(up(256 + int(counts[2]) * cfg.head_size_v * 2) +
                                       int(counts[2]) * 4)
     # nothing past the counts was written
     assert (work[n:] == -7).all() and (comb[m:] == -7).all()

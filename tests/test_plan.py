@@ -79,9 +79,9 @@ def test_plan_matches_oracle_plan(lib, oracle_mod, seed):
     assert np.array_equal(plan.work, work)
     assert np.array_equal(plan.combine, comb)
     check_partition(c, ctx, ql, plan)
-    # workspace: status area, then P*hv fp32 partials, then P fp32 lse, 256-aligned parts
+    # workspace: status area, then P*hv fp16 partials, then P fp32 lse, 256-aligned parts
     up = lambda x: (x + 255) // 256 * 256
-    assert plan.workspace_bytes == up(up(256 + prows * hv * 4) + prows * 4)
+    assert plan.workspace_bytes == up(up(256 + prows * hv * 2) + prows * 4)
 
 
 def test_named_workload_plans(lib, oracle_mod):
