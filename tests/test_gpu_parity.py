@@ -308,6 +308,36 @@ def test_tensor_core_parity(oracle_mod, name):
     full_parity(oracle_mod, TC_CASES[name]())
 
 
+# More than 32 splits of one tile (1-block chunks over long sequences): the
+# combine's second round of partial-row loads and its weights past the 32 that
+# a warp's lanes hold, in its 4-dims-a-lane form (value heads of 128) and its
+# 8-dims-a-lane form (256 and 512), after each kernel family's fp16 partials.
+SPLIT_CASES = {
+    "fma_hd128_bs16": lambda: W.make_workload("s1", context_lens=[700, 20], num_heads=2,
+                                              kv_heads=2, head_size_k=128, block_size=16,
+                                              seed=60, chunk_blocks=1),
+    "mma_hd128_gqa": lambda: W.make_workload("s2", context_lens=[5000, 130], num_heads=8,
+                                             kv_heads=2, head_size_k=128, block_size=128,
+                                             seed=61, chunk_blocks=1),
+    "tc_mqa_hd512": lambda: W.make_workload("s3", context_lens=[4300, 300], num_heads=64,
+                                            kv_heads=1, head_size_k=512, block_size=128,
+                                            std=0.5, seed=62, chunk_blocks=1),
+    "wide_hd256_shared": lambda: W.make_workload("s4", context_lens=[2500, 70], num_heads=16,
+                                                 kv_heads=1, head_size_k=256, block_size=64,
+                                                 seed=63, chunk_blocks=1, shared_kv=True),
+    "wide_mla_shared": lambda: W.make_workload("s5", context_lens=[2200, 33], num_heads=16,
+                                               kv_heads=1, head_size_k=576, head_size_v=512,
+                                               block_size=64, seed=64, chunk_blocks=1,
+                                               shared_kv=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SPLIT_CASES))
+def test_many_splits_parity(oracle_mod, name):
+    _, db = full_parity(oracle_mod, SPLIT_CASES[name]())
+    assert int(np.asarray(db.plan.combine)[:, 3].max()) > 32
+
+
 def test_tensor_core_split_and_unsplit_agree(oracle_mod):
     w = TC_CASES["tc_mqa_hd512"]()
     a, _ = run_gpu(w, chunk_blocks=1)
