@@ -102,7 +102,9 @@ __global__ void __launch_bounds__(128) fma_decode_kernel(const __grid_constant__
   const int kxor = (t >> ksh) & kmask;
   const int nkc = hk / 16;  // K chunks per half
   const int vchunks = hv / 8;
-  const int lpt = vchunks >= 32 ? 32 : (vchunks > 8 ? 16 : (vchunks > 4 ? 8 : (vchunks > 2 ? 4 : 2)));
+  // lanes per token: the smallest power of two that covers the V chunks (at
+  // most 32; beyond 32 chunks a lane takes chunks cl, cl + 32, ...)
+  const int lpt = vchunks > 16 ? 32 : (vchunks > 8 ? 16 : (vchunks > 4 ? 8 : (vchunks > 2 ? 4 : 2)));
   const int ng = 32 / lpt, grp = lane / lpt, cl = lane % lpt;
 
   float m_run[RT], l_run[RT];

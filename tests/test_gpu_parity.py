@@ -79,6 +79,16 @@ CASES = {
     "hk80_hv48": lambda: W.make_workload("hk80", context_lens=[50, 211], num_heads=2,
                                          kv_heads=2, head_size_k=80, head_size_v=48,
                                          block_size=16, seed=7),
+    # value heads of 17-31 eight-dim chunks (144-240 dims) on the CUDA-core
+    # kernel: one lane per chunk (found by the random shapes, where 16 lanes
+    # left dims 128 and up unaccumulated)
+    "hk192_shared_alibi": lambda: W.make_workload("hk192", context_lens=[418, 99], num_heads=2,
+                                                  kv_heads=2, head_size_k=192, block_size=48,
+                                                  mask_type=W.MASK_ALIBI, shared_kv=True,
+                                                  seed=8, chunk_blocks=2),
+    "hk160_hv224": lambda: W.make_workload("hk160", context_lens=[300, 77, 129], num_heads=6,
+                                           kv_heads=3, head_size_k=160, head_size_v=224,
+                                           block_size=32, seed=9),
     "hk256_g8": lambda: W.make_workload("g8", context_lens=[1, 2, 15, 16, 17, 255, 256, 257],
                                         num_heads=16, kv_heads=2, head_size_k=256,
                                         block_size=128, seed=8),

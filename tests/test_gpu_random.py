@@ -1,0 +1,116 @@
+"""Seeded random shapes against the oracle.
+
+Each case is drawn from one kernel family (the CUDA-core and warp-MMA decode
+kernels for up to 8 rows per kv head, the 16-row shared-KV kernel, the tcgen05
+decode kernel for up to 64 rows, the prefill kernels beyond 64) with its
+head sizes, block size, query lengths, mask, cache layout and chunking drawn
+at random within the limits of pa.h, and compared element by element with the
+fp64 oracle. The CPU test checks that every drawn case plans and that the
+draw covers every family and option; the GPU test runs them.
+"""
+import numpy as np
+import pytest
+
+import paged_kv_cache_206_gb300 as pa
+from paged_kv_cache_206_gb300 import build_lib
+from paged_kv_cache_206_gb300 import workloads as W
+
+N_CASES = 36
+SEED = 2026
+
+
+def _family(G, maxq, hk, hv, shared):
+    rows = G * maxq
+    if rows <= 8:
+        return "warp"
+    if rows > 64 and hk == hv and hk in (64, 128):
+        return "prefill"
+    if rows <= 16 and shared and ((hk, hv) == (576, 512) or (hk == hv and hk in (256, 512))):
+        return "wide"
+    return "tc"
+
+
+def draw(i):
+    """Keyword arguments of workloads.make_workload for case i, and its family."""
+    rng = np.random.default_rng([SEED, i])
+    fam = ["warp", "warp", "tc", "wide", "prefill"][i % 5]
+    shared = False
+    if fam == "warp":
+        G = int(rng.choice([1, 2, 4, 8]))
+        q = int(rng.choice([1, 1, 2])) if G <= 4 else 1
+        if G * q > 8:
+            q = 1
+        hk, hv = [(64, 64), (80, 48), (96, 96), (128, 128), (192, 192), (256, 256), (512, 512),
+                  (576, 512)][int(rng.integers(0, 8))]
+        shared = hv <= hk and bool(rng.random() < 0.3)
+    elif fam == "tc":
+        G, q = [(16, 1), (24, 1), (32, 1), (64, 1), (16, 2), (8, 4), (12, 3)][int(rng.integers(0, 7))]
+        hk, hv = [(128, 128), (256, 256), (512, 512), (576, 512)][int(rng.integers(0, 4))]
+        shared = bool(rng.random() < 0.3) and G * q > 16  # 16-row shared caches go to the wide kernel
+    elif fam == "wide":
+        G, q = [(16, 1), (12, 1), (8, 2), (10, 1)][int(rng.integers(0, 4))]
+        hk, hv = [(576, 512), (256, 256), (512, 512)][int(rng.integers(0, 3))]
+        shared = True
+    else:
+        G = int(rng.choice([1, 2, 4]))
+        hk = hv = int(rng.choice([64, 128]))
+        q = int(rng.integers(70, 200)) if G == 1 else int(rng.integers(20, 90))
+        if G * q <= 64:
+            q = 65 // G + 1
+    kv_heads = int(rng.choice([1, 2]))
+    bs_choices = [16, 32, 48, 64, 128] if (q == 1 and max(hk, hv) <= 256) else [16, 32, 64, 128]
+    bs = int(rng.choice(bs_choices))
+    B = int(rng.integers(2, 4))
+    lens = [int(rng.integers(q, q + 600)) for _ in range(B)]
+    if fam == "prefill" and rng.random() < 0.5:
+        lens = [q] * B  # q = L: PA_ENCODER-style prefill
+    masks = [W.MASK_NONE, W.MASK_ALIBI, W.MASK_NORM_COMPRESS, W.MASK_NORM]
+    mask = int(masks[int(rng.integers(0, 4))])
+    chunk = int(rng.choice([0, 0, 1, 2, 5]))
+    kw = dict(context_lens=lens, q_seqlens=q, num_heads=G * kv_heads, kv_heads=kv_heads,
+              head_size_k=hk, head_size_v=hv, block_size=bs, mask_type=mask,
+              seed=1000 + i, chunk_blocks=chunk, shared_kv=shared,
+              std=0.5 if max(hk, hv) >= 256 else 1.0)
+    assert _family(G, q, hk, hv, shared) == fam, (i, fam, G, q, hk, hv, shared)
+    return kw, fam
+
+
+def make(i):
+    kw, _ = draw(i)
+    return W.make_workload(f"rand{i}", **kw)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return pa.load_library()
+
+
+def test_random_cases_plan_and_cover(lib):
+    """Every drawn case is valid for pa_plan, and the draw spans every kernel
+    family, mask type, shared and separate caches, splits and no splits."""
+    fams, masks, shared, split, unsplit = set(), set(), set(), False, False
+    for i in range(N_CASES):
+        kw, fam = draw(i)
+        w = W.make_workload(f"rand{i}", **kw)
+        cfg = pa.config_for(w, num_sms=152)
+        ql = None if np.all(w.q_seqlens == 1) else w.q_seqlens
+        plan = pa.pa_plan(cfg, w.context_lens, ql)
+        fams.add(fam)
+        masks.add(kw["mask_type"])
+        shared.add(kw["shared_kv"])
+        split |= plan.combine.shape[0] > 0
+        unsplit |= plan.combine.shape[0] == 0
+    assert fams == {"warp", "tc", "wide", "prefill"}
+    assert masks == {W.MASK_NONE, W.MASK_ALIBI, W.MASK_NORM_COMPRESS, W.MASK_NORM}
+    assert shared == {True, False} and split and unsplit
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_case_parity(lib, oracle_mod, i):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tests.test_gpu_parity import full_parity
+    full_parity(oracle_mod, make(i))
