@@ -80,6 +80,87 @@ def make(i):
     return W.make_workload(f"rand{i}", **kw)
 
 
+# A wider draw: any head sizes the kernels take (multiples of 16 up to 576, K
+# and V apart for up to 8 rows a kv head), block sizes 16-256, batches of 1-4,
+# lengths on and around block boundaries and past the 2048 of the compressed
+# mask, extra block-table columns.
+N_WIDE = 160
+TC_HEADS = [(128, 128), (256, 256), (512, 512), (576, 512)]
+
+
+def _supported(rows, hk, hv):
+    if rows <= 8:
+        return True
+    if rows > 64 and hk == hv and hk in (64, 128):
+        return True
+    return (hk, hv) in TC_HEADS
+
+
+def draw_wide(i):
+    rng = np.random.default_rng([SEED + 1, i])
+    while True:
+        kind = int(rng.integers(0, 4))
+        if kind == 0:      # up to 8 rows a kv head: any head sizes
+            G = int(rng.choice([1, 2, 3, 4, 5, 8]))
+            q = int(rng.choice([1, 1, 1, 2])) if G <= 4 else 1
+            if G >= 2 and rng.random() < 0.3:  # the warp-MMA kernel's head sizes
+                hk, hv = [(64, 64), (128, 128), (256, 256), (512, 512), (576, 512)][int(rng.integers(0, 5))]
+            else:
+                hk = 16 * int(rng.integers(1, 37))
+                hv = 16 * int(rng.integers(1, 37)) if rng.random() < 0.4 else hk
+        elif kind == 1:    # 9-64 rows: the tensor-core head sizes
+            G, q = [(9, 1), (16, 1), (17, 1), (24, 1), (33, 1), (48, 1), (64, 1), (5, 2), (16, 3),
+                    (8, 8), (21, 3)][int(rng.integers(0, 11))]
+            hk, hv = TC_HEADS[int(rng.integers(0, 4))]
+        elif kind == 2:    # prefill-like: more than 64 rows
+            G = int(rng.choice([1, 2, 4, 8]))
+            q = int(rng.integers(65 // G + 1, 65 // G + 120))
+            hk = hv = int(rng.choice([64, 128, 128, 256, 512]))
+        else:              # 9-16 rows over a shared cache
+            G, q = [(9, 1), (16, 1), (8, 2), (5, 3)][int(rng.integers(0, 4))]
+            hk, hv = [(576, 512), (256, 256), (512, 512), (128, 128)][int(rng.integers(0, 4))]
+        rows = G * q
+        if max(hk, hv) > PA_MAX_HEAD or not _supported(rows, hk, hv):
+            continue
+        shared = hv <= hk and (kind == 3 or bool(rng.random() < 0.25))
+        big = max(hk, hv) > 256 or q > 1
+        bs = int(rng.choice([16, 32, 48, 64, 80, 112, 128] + ([] if big else [144, 256])))
+        B = int(rng.integers(1, 5))
+        lens = []
+        for _ in range(B):
+            r = rng.random()
+            if r < 0.2:
+                L = q  # only the query tokens
+            elif r < 0.4:
+                L = max(q, bs * int(rng.integers(1, 6)) + int(rng.integers(-1, 2)))  # around a block edge
+            elif r < 0.47 and q <= 8:
+                L = int(rng.integers(2049, 2300))  # past the compressed mask's 2048
+            else:
+                L = int(rng.integers(q, q + 700))
+            lens.append(max(L, q))
+        masks = [W.MASK_NONE, W.MASK_ALIBI, W.MASK_NORM_COMPRESS, W.MASK_NORM]
+        mask = int(masks[int(rng.integers(0, 4))])
+        kw = dict(context_lens=lens, q_seqlens=q, num_heads=G * int(rng.choice([1, 2])),
+                  head_size_k=hk, head_size_v=hv, block_size=bs, mask_type=mask,
+                  seed=5000 + i, chunk_blocks=int(rng.choice([0, 0, 1, 2, 3, 7])),
+                  shared_kv=shared, extra_table_cols=int(rng.choice([0, 0, 3])),
+                  std=0.5 if max(hk, hv) >= 256 else 1.0)
+        kw["kv_heads"] = kw["num_heads"] // G
+        return kw
+
+
+PA_MAX_HEAD = 576
+
+
+def test_wide_random_cases_plan(lib):
+    """Every case of the wider draw is valid for pa_plan."""
+    for i in range(N_WIDE):
+        w = W.make_workload(f"wide{i}", **draw_wide(i))
+        cfg = pa.config_for(w, num_sms=152)
+        ql = None if np.all(w.q_seqlens == 1) else w.q_seqlens
+        pa.pa_plan(cfg, w.context_lens, ql)
+
+
 @pytest.fixture(scope="module")
 def lib():
     build_lib.build()
@@ -114,3 +195,13 @@ def test_random_case_parity(lib, oracle_mod, i):
         pytest.skip("no CUDA device")
     from tests.test_gpu_parity import full_parity
     full_parity(oracle_mod, make(i))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("i", range(N_WIDE))
+def test_wide_random_case_parity(lib, oracle_mod, i):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tests.test_gpu_parity import full_parity
+    full_parity(oracle_mod, W.make_workload(f"wide{i}", **draw_wide(i)))
