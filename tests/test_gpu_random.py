@@ -205,3 +205,31 @@ def test_wide_random_case_parity(lib, oracle_mod, i):
         pytest.skip("no CUDA device")
     from tests.test_gpu_parity import full_parity
     full_parity(oracle_mod, W.make_workload(f"wide{i}", **draw_wide(i)))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("i", range(24))
+def test_planned_paths_agree_bit_for_bit(lib, i):
+    """The device planner's step (capacity grids, CTAs past the device counts
+    leaving at once) and the recorded graph step (pinned host arena, device
+    plan, output straight into pinned memory when small) give the host-planned
+    step's output bit for bit: the same lists, the same kernels."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = W.make_workload(f"wide{i}", **draw_wide(i))
+    db = pa.DeviceBatch(w)
+    host = db.forward().clone().cpu()
+    step = pa.DevicePlanStep(db)
+    dev = step.run().clone().cpu()
+    assert step.status()[0] == pa.PA_OK
+    gs = pa.GraphStep(db.cfg, db.key_cache, db.value_cache, w.total_q, mask=db.mask,
+                      alibi_slopes=db.alibi_slopes)
+    gs.block_tables.copy_(torch.from_numpy(np.ascontiguousarray(w.block_tables)))
+    if gs.q_seqlens is not None:
+        gs.q_seqlens.copy_(torch.from_numpy(np.ascontiguousarray(w.q_seqlens)))
+    gs.context_lens.copy_(torch.from_numpy(np.ascontiguousarray(w.context_lens)))
+    gs.query.copy_(torch.from_numpy(np.ascontiguousarray(w.query)))
+    graph = gs.run().clone()
+    assert gs.status()[0] == pa.PA_OK
+    assert torch.equal(host, dev) and torch.equal(host, graph)
