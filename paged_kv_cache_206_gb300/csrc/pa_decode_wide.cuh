@@ -199,6 +199,10 @@ __global__ void __launch_bounds__(kWideThreads, 1) wide_decode_kernel(
             }
             ++issued;
           }
+          // tiles 0 and 1 first: at the start of a wave every CTA's ring is
+          // empty, and the first tile would otherwise queue behind the third
+          // of every CTA (tile 2 is issued once tile 0 has landed)
+          if (ok && n == 1 && ntiles > 2) ok = mbar_wait(&full[0], 0, P.wait_limit);
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       }
