@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 
 import numpy as np
@@ -22,9 +23,20 @@ _OUT = os.path.join(_HERE, "_build", "liboracle.so")
 _lib = None
 
 
+def _stamp() -> str:
+    """The machine and compiler the library is built for: one built elsewhere
+    is never reused."""
+    ver = subprocess.run(["gcc", "--version"], capture_output=True, text=True).stdout
+    return platform.machine() + " " + ver.splitlines()[0] if ver else platform.machine()
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle if its shared library is missing or stale."""
-    if (not force and os.path.exists(_OUT)
+    """Compile the oracle if its shared library is missing, stale, or built for
+    another machine or compiler."""
+    stamp_path = _OUT + ".stamp"
+    stamp = _stamp()
+    same = os.path.exists(stamp_path) and open(stamp_path).read().strip() == stamp
+    if (not force and same and os.path.exists(_OUT)
             and os.path.getmtime(_OUT) >= os.path.getmtime(_SRC)):
         return _OUT
     os.makedirs(os.path.dirname(_OUT), exist_ok=True)
@@ -32,6 +44,8 @@ def build(force: bool = False) -> str:
     subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC,
                     "-o", tmp, "-lm"], check=True)
     os.replace(tmp, _OUT)
+    with open(stamp_path, "w") as f:
+        f.write(stamp + "\n")
     return _OUT
 
 

@@ -2,14 +2,18 @@
 
 Each translation unit under ``csrc/`` compiles in parallel to an object under
 ``_build/obj``; the objects link into ``_build/libpa.so``. Nothing is rebuilt
-when every object is newer than its source and every header. The CUDA runtime
+when every object is newer than its source and every header, and the build
+stamp (machine, compiler version, flags) matches the one the objects were made
+with; objects from another machine or compiler are never reused. The CUDA runtime
 is linked statically and the driver is reached through the runtime's
 entry-point query, so the library loads on a machine without a GPU.
 """
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
@@ -43,10 +47,22 @@ def _headers_mtime() -> float:
     return max(os.path.getmtime(h) for h in hs)
 
 
+def _stamp(cc: str) -> str:
+    """What the objects depend on beyond their sources: the machine, the
+    compiler and the flags."""
+    ver = subprocess.run([cc, "--version"], capture_output=True, text=True).stdout
+    text = "\n".join([platform.machine(), ver, " ".join(FLAGS), " ".join(ARCH)])
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -> str:
     """Compile what is stale and link; returns the library path."""
     os.makedirs(os.path.join(BUILD, "obj"), exist_ok=True)
     cc = nvcc()
+    stamp_path = os.path.join(BUILD, "stamp")
+    stamp = _stamp(cc)
+    if not os.path.exists(stamp_path) or open(stamp_path).read().strip() != stamp:
+        force = True  # objects (if any) from another machine, compiler or flag set
     hdr = _headers_mtime()
     objs, todo = [], []
     for src in sources():
@@ -81,6 +97,8 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
         if r.returncode != 0:
             raise RuntimeError(f"link of libpa.so failed:\n{r.stderr}")
         os.replace(tmp, LIB)
+        with open(stamp_path, "w") as f:
+            f.write(stamp + "\n")
     return LIB
 
 
